@@ -1,0 +1,338 @@
+"""Benchmark of the DeepSeekMoE layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = one moe_layer_forward over T tokens of the chosen workload (default: the 16B-like layer,
+T = 16384, d = 2048, 2 shared + 64 routed experts of width 1408, top-6): router, permutation,
+gather, gate/up and down expert GEMMs, combine and balance statistics. Inputs are seeded
+synthetic tensors of the workload's shape, resident in HBM when the timed region starts. Each
+step is timed on its own with CUDA events on the launching stream; L2 is flushed (a 512 MB
+write) between steps, outside the timed events. Under torchrun every rank runs its own batch of
+T tokens (independent replicas, weak scaling); the reported time is the maximum over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on bounded samples of the same workload instead.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import moe_inputs  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s at 16B-like shape"
+UNIT = "tokens/s"
+
+
+def flops_per_token(sh) -> float:
+    """Algorithmic FLOPs per token: router 2*d*N', and three GEMMs of 2*d*I per active expert."""
+    return 6.0 * sh.d * sh.inter * (sh.n_shared + sh.top_k) + 2.0 * sh.d * sh.n_routed
+
+
+def gate_up_flops(sh, T) -> float:
+    return 4.0 * sh.d * sh.inter * T * (sh.n_shared + sh.top_k)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained"), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+# ------------------------------------------------------------------------------ clocks ----
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="moe_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- reference ----
+
+def oracle_sample_rate(sh, n_tokens: int, seed: int = 0):
+    """Oracle tokens/s on n_tokens of the workload (each token routed on its own, all its
+    experts applied, fp64). Returns (tokens/s, seconds, threads)."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    cfg = oracle.OracleCfg.from_shape(sh, T=n_tokens)
+    inputs = moe_inputs.make_inputs(sh, T=n_tokens, seed=sh.seed + 1000 + seed)
+    t0 = time.perf_counter()
+    oracle.forward_tokens(cfg, inputs, np.arange(n_tokens))
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt, oracle.threads()
+
+
+def run_reference(args, sh, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    n_tok = max(1, int(args.ref_tokens))
+    cfg = oracle.OracleCfg.from_shape(sh, T=n_tok)
+    inputs = moe_inputs.make_inputs(sh, T=n_tok, seed=sh.seed + 1000)
+    toks = np.arange(n_tok)
+    for _ in range(args.warmup):
+        oracle.forward_tokens(cfg, inputs, toks)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.forward_tokens(cfg, inputs, toks)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = n_tok * args.steps / total
+    sample = (f"{n_tok} tokens of the {sh.name} workload per step (per-token routing over "
+              f"{sh.n_routed} experts + {sh.n_shared + sh.top_k} SwiGLU experts, fp64)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": sh.name, "T": sh.T, "d": sh.d, "n_shared": sh.n_shared,
+                   "n_routed": sh.n_routed, "inter": sh.inter, "top_k": sh.top_k},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------------------- ours ----
+
+def run_ours(args, sh, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import fine_grained_moe_softmax_b300 as moe
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    T = sh.T
+    inputs = moe_inputs.make_inputs(sh, seed=sh.seed + 7919 * rank)
+    cfg = moe.MoEConfig.from_shape(sh)
+    layer = moe.MoELayer(cfg, inputs["centroids"], inputs["w_gate"], inputs["w_up"],
+                         inputs["w_down"], inputs["bias"], device=dev)
+    u_host = inputs["u"].pin_memory()
+    u = u_host.to(dev)
+    del inputs
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        layer.forward(u)
+    torch.cuda.synchronize(dev)
+    status = layer.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {moe.moe_status_string(status)} after warm-up")
+
+    # ---- device-resident timing: every step timed on its own, L2 flushed in between ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    moe.moe_profile_enable(True, args.steps)
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = moe.moe_launch_count()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        layer.forward(u)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = moe.moe_launch_count() - launches0
+    stage_ms, n_prof = moe.moe_profile_read()
+    moe.moe_profile_enable(False)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+
+    # ---- end to end through host buffers: H2D of u, the layer, D2H of h and the losses ----
+    h_host = torch.empty(T, sh.d, dtype=u.dtype).pin_memory()
+    loss_host = torch.empty(2, dtype=torch.float32).pin_memory()
+    u_dev = torch.empty_like(u)
+
+    def e2e_step():
+        u_dev.copy_(u_host, non_blocking=True)
+        layer.forward(u_dev)
+        h_host.copy_(layer.h, non_blocking=True)
+        loss_host.copy_(layer.losses, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e_starts[i].record(stream)
+        e2e_step()
+        e_ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends))
+    status = layer.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {moe.moe_status_string(status)} after timing")
+
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = t.tolist()
+    if rank != 0:
+        return
+
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = load_peaks()
+    tokens = T * world * args.steps
+    value = tokens / (total_ms / 1e3)
+    e2e_value = tokens / (e2e_ms / 1e3)
+    gu_ms = stage_ms["gemm_gate_up"] / max(n_prof, 1)
+    gu_tflops = gate_up_flops(sh, T) / (gu_ms / 1e3) / 1e12
+    layer_tflops = flops_per_token(sh) * T / (total_ms / args.steps / 1e3) / 1e12
+    traffic = None
+    prof_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof_path):
+        with open(prof_path) as f:
+            traffic = json.load(f).get(sh.name, {}).get("gemm_gate_up_bytes")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": sh.dtype, "data": "synthetic",
+        "config": {"workload": sh.name, "T": T, "d": sh.d, "n_shared": sh.n_shared,
+                   "n_routed": sh.n_routed, "inter": sh.inter, "top_k": sh.top_k,
+                   "global_batch": T * world, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (512 MB write outside the events)",
+                   "inputs": "seeded Gaussian tensors of the workload's shape"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel (gate/up + SwiGLU epilogue)",
+                     "achieved": gu_tflops, "peak": bf16_tf, "unit": "TFLOP/s",
+                     "frac": gu_tflops / bf16_tf, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 burst"},
+        "layer_roofline": {"achieved_tflops": layer_tflops, "frac_of_bf16_peak":
+                           layer_tflops / bf16_tf, "flops_per_token": flops_per_token(sh)},
+        "stage_ms_per_step": {k: v / max(n_prof, 1) for k, v in stage_ms.items()},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * sh.d * u.element_size(),
+                "d2h_bytes_per_step": T * sh.d * u.element_size() + 8},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_tokens
+        rate, secs, threads = oracle_sample_rate(sh, n)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"{n} tokens of the {sh.name} workload, fp64 oracle, "
+                                          f"{secs:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="16b_bf16", choices=sorted(moe_inputs.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=512)
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    sh = moe_inputs.CONFIGS[args.config]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, sh, rank, world)
+        else:
+            run_ours(args, sh, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,157 @@
+// combine.cu -- gated combine with the residual, and the balance statistics.
+//
+// [P1] "DeepSeekMoE 论文解读" (xxmr.cn), §方法细节: h_t = sum_i g_{i,t} FFN_i(u_t) + u_t, with the
+//      shared experts always active (gate 1); L_ExpBal = a1 sum_i f_i P_i; L_DevBal = a2 sum over
+//      D groups of routed experts (one group per device).
+// [P2] "【论文总结】MoE" (mickeyding.github.io), §2.3: f_i uses the factor N'/K' so the loss does not
+//      depend on the expert count; §2.4: f'_i is the mean usage frequency of group i's experts and
+//      P'_i the group's affinity (read here as the sum of P over the group).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+template <typename E> struct Vec;   // 16-byte vector of E
+template <> struct Vec<float> {
+    static constexpr int n = 4;
+    __device__ static void load(const void* p, float* x) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    }
+    __device__ static void store(void* p, const float* x) {
+        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+};
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int n = 8;
+    __device__ static void load(const void* p, float* x) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(h[q]);
+            x[2 * q] = f.x;
+            x[2 * q + 1] = f.y;
+        }
+    }
+    __device__ static void store(void* p, const float* x) {
+        uint4 v;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
+        *reinterpret_cast<uint4*>(p) = v;
+    }
+};
+
+// One warp per token; each lane owns 16-byte column vectors. fp32 accumulation in the fixed
+// order u, shared sum, routed k = 0..K'-1.
+template <typename E>
+__global__ void combine_kernel(Dims m, const E* __restrict__ u, const E* __restrict__ y_r,
+                               const E* __restrict__ y_s, const int* __restrict__ perm_slot,
+                               const float* __restrict__ gate, E* __restrict__ h, int* status) {
+    constexpr int VN = Vec<E>::n;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (t >= m.T) return;
+    const long TK = (long)m.T * m.K;
+    int rows[kMaxTopK];
+    float g[kMaxTopK];
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k) {
+        rows[k] = -1;
+        g[k] = 0.f;
+        if (k < m.K) {
+            rows[k] = perm_slot[(size_t)t * m.K + k];
+            g[k] = gate[(size_t)t * m.K + k];
+            if (rows[k] < 0 || rows[k] >= TK) { bad = true; rows[k] = -1; }
+        }
+    }
+    if (bad && lane == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
+    for (int c = lane * VN; c < m.d; c += 32 * VN) {
+        float acc[VN], y[VN];
+        Vec<E>::load(u + (size_t)t * m.d + c, acc);
+        if (m.Ks > 0) {
+            Vec<E>::load(y_s + (size_t)t * m.d + c, y);
+#pragma unroll
+            for (int q = 0; q < VN; ++q) acc[q] += y[q];
+        }
+#pragma unroll
+        for (int k = 0; k < kMaxTopK; ++k) {
+            if (k < m.K && rows[k] >= 0) {
+                Vec<E>::load(y_r + (size_t)rows[k] * m.d + c, y);
+#pragma unroll
+                for (int q = 0; q < VN; ++q) acc[q] = fmaf(g[k], y[q], acc[q]);
+            }
+        }
+        Vec<E>::store(h + (size_t)t * m.d + c, acc);
+    }
+}
+
+// One CTA; thread j handles expert j, thread 0 sums in expert order.
+__global__ void balance_kernel(Dims m, const int* __restrict__ counts,
+                               const float* __restrict__ psum, float* __restrict__ f_out,
+                               float* __restrict__ P_out, float* __restrict__ losses) {
+    __shared__ float f_s[kMaxRouted], P_s[kMaxRouted];
+    const int N = m.N;
+    const float Tf = (float)max(m.T, 1);
+    const float scale = (float)N / ((float)m.K * Tf);
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        const float f = scale * (float)counts[j];
+        const float P = psum[j] / Tf;
+        f_s[j] = f;
+        P_s[j] = P;
+        f_out[j] = f;
+        P_out[j] = P;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float lexp = 0.f;
+        for (int j = 0; j < N; ++j) lexp += f_s[j] * P_s[j];
+        float ldev = 0.f;
+        const int base = N / m.D, extra = N % m.D;
+        int first = 0;
+        for (int g = 0; g < m.D; ++g) {
+            const int size = base + (g < extra ? 1 : 0);
+            float fs = 0.f, ps = 0.f;
+            for (int j = first; j < first + size; ++j) {
+                fs += f_s[j];
+                ps += P_s[j];
+            }
+            ldev += (fs / (float)size) * ps;
+            first += size;
+        }
+        losses[0] = m.a1 * lexp;
+        losses[1] = m.a2 * ldev;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Dims& m, const void* u, const void* y_r, const void* y_s,
+                           const int* perm_slot, const float* gate, void* h, int* status,
+                           cudaStream_t st) {
+    if (m.T == 0) return cudaSuccess;
+    const int threads = 256, blocks = (m.T + threads / 32 - 1) / (threads / 32);
+    if (m.dtype == MOE_DTYPE_F32)
+        combine_kernel<float><<<blocks, threads, 0, st>>>(
+            m, static_cast<const float*>(u), static_cast<const float*>(y_r),
+            static_cast<const float*>(y_s), perm_slot, gate, static_cast<float*>(h), status);
+    else
+        combine_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
+            m, static_cast<const __nv_bfloat16*>(u), static_cast<const __nv_bfloat16*>(y_r),
+            static_cast<const __nv_bfloat16*>(y_s), perm_slot, gate,
+            static_cast<__nv_bfloat16*>(h), status);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_balance(const Dims& m, const int* counts, const float* psum, float* f,
+                          float* P, float* losses, cudaStream_t st) {
+    balance_kernel<<<1, 256, 0, st>>>(m, counts, psum, f, P, losses);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

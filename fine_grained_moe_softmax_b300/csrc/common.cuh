@@ -1,0 +1,124 @@
+// common.cuh -- shared device/host definitions of the MoE layer library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_b300.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------- layout ----
+
+// Problem dimensions after validation (all int; sizes fit in int32 by the supported limits).
+struct Dims {
+    int T, d, Ks, N, I, K, renorm, D;
+    float a1, a2;
+    int dtype;  // MOE_DTYPE_F32 / MOE_DTYPE_BF16
+    __host__ __device__ int elem() const { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
+};
+
+constexpr int kRouteTile = 128;   // tokens per router / permutation tile
+constexpr int kMaxRouted = 256;   // N' limit
+constexpr int kMaxTopK = 16;      // K' limit
+
+// Byte offsets of every scratch region inside the caller's workspace (256-byte aligned).
+struct WsLayout {
+    size_t status;        // int32 status word (+ padding)
+    size_t tile_counts;   // [n_tiles, N] int32: per router tile, tokens choosing expert j
+    size_t tile_psum;     // [n_tiles, N] fp32: per router tile, sum of affinities
+    size_t tile_base;     // [n_tiles, N] int32: first permuted row of tile's tokens for expert j
+    size_t psum;          // [N] fp32   (layer forward)
+    size_t offsets;       // [N+1] int32 (layer forward)
+    size_t perm_token;    // [T*K] int32 (layer forward)
+    size_t perm_slot;     // [T*K] int32 (layer forward)
+    size_t x_perm;        // [T*K, d] elem: token rows in permuted order
+    size_t act_r;         // [T*K, I] elem: routed SwiGLU activations
+    size_t act_s;         // [T, Ks*I] elem: shared SwiGLU activations
+    size_t y_r;           // [T*K, d] elem (layer forward)
+    size_t y_s;           // [T, d] elem (layer forward)
+    size_t total;
+    int n_tiles;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(const Dims& m) {
+    WsLayout L{};
+    const size_t TK = (size_t)m.T * m.K, e = (size_t)m.elem();
+    L.n_tiles = (m.T + kRouteTile - 1) / kRouteTile;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+    L.status = take(256);
+    L.tile_counts = take((size_t)L.n_tiles * m.N * 4);
+    L.tile_psum = take((size_t)L.n_tiles * m.N * 4);
+    L.tile_base = take((size_t)L.n_tiles * m.N * 4);
+    L.psum = take((size_t)m.N * 4);
+    L.offsets = take((size_t)(m.N + 1) * 4);
+    L.perm_token = take(TK * 4);
+    L.perm_slot = take(TK * 4);
+    L.x_perm = take(TK * m.d * e);
+    L.act_r = take(TK * m.I * e);
+    L.act_s = take((size_t)m.T * m.Ks * m.I * e);
+    L.y_r = take(TK * m.d * e);
+    L.y_s = take((size_t)m.T * m.d * e);
+    L.total = o;
+    return L;
+}
+
+// Packed expert weights (element offsets). Gate/up rows are interleaved in blocks of 16: packed
+// row 32*b + q holds gate row 16*b + q for q < 16 and up row 16*b + q - 16 otherwise, so any
+// 32-column slice of a gate/up product holds 16 gate values and their 16 matching up values.
+struct PackLayout {
+    size_t gu_r;   // [N, 2I, d]
+    size_t gu_s;   // [2*Ks*I, d]   shared experts side by side (one expert of width Ks*I)
+    size_t dn_r;   // [N, d, I]
+    size_t dn_s;   // [d, Ks*I]
+    size_t total;  // elements
+};
+
+inline PackLayout pack_layout(const Dims& m) {
+    PackLayout P{};
+    const size_t Id = (size_t)m.I * m.d;
+    P.gu_r = 0;
+    P.gu_s = P.gu_r + (size_t)m.N * 2 * Id;
+    P.dn_r = P.gu_s + (size_t)m.Ks * 2 * Id;
+    P.dn_s = P.dn_r + (size_t)m.N * Id;
+    P.total = P.dn_s + (size_t)m.Ks * Id;
+    return P;
+}
+
+// ------------------------------------------------------------------------ device utils ----
+
+// First error wins; later errors leave the word alone.
+__device__ __forceinline__ void set_status(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+template <typename E> __device__ __forceinline__ float to_f32(E x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename E> __device__ __forceinline__ E from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float silu_f32(float a) { return a / (1.0f + __expf(-a)); }
+
+// ------------------------------------------------------------------------ host helpers ----
+
+// Counts every kernel launch made through the library (moe_launch_count).
+void note_launches(int n);
+int sm_count();  // multiprocessors of the current device (cached per device)
+
+}  // namespace moe

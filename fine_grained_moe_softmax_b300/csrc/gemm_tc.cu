@@ -1,0 +1,459 @@
+// gemm_tc.cu -- grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Expert FFN ([P1] "DeepSeekMoE 论文解读" (xxmr.cn), §方法细节, read as SwiGLU):
+//   gate/up:  act = silu(A W_gate^T) * (A W_up^T)  (SwiGLU formed in the epilogue)
+//   down:     y   = act W_down^T
+// over one dense shared group (all T tokens; the K_s shared experts side by side) and N' routed
+// groups (expert j: rows offsets[j] .. offsets[j+1]-1 of the permuted matrices).
+//
+// Kernel shape: persistent, one CTA per SM, 6 warps.
+//   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] (bf16, 128-byte swizzle) per
+//               stage into a STAGES-deep shared-memory ring.
+//   warp 1      allocates 2*BN TMEM columns; one thread issues tcgen05.mma (M=128, N=BN, K=16)
+//               into one of two fp32 accumulators, and commits stage releases and tile completion
+//               to mbarriers.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes 32*(w%4)..),
+//               SwiGLU or plain conversion to bf16, direct global stores of valid rows/columns.
+// Two accumulators let the epilogue of tile i overlap the main loop of tile i+1. Every wait on an
+// mbarrier is bounded in time; on expiry the kernel records MOE_ERR_TIMEOUT, stops issuing work,
+// drains what it issued and frees its TMEM before returning.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "groups.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+cudaError_t launch_expert_gemms_simt(const Dims& m, const void* u, const void* x_perm,
+                                     const void* packed, const int* offsets, void* act_r,
+                                     void* act_s, void* y_r, void* y_s, cudaStream_t st,
+                                     cudaEvent_t mid_event);
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle row
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
+
+struct TcArgs {
+    CUtensorMap a_r, a_s, b_r, b_s;
+    const int* offsets;
+    GroupTiles gt;
+    int k_blocks_r, k_blocks_s;
+    int b_rows_per_expert;
+    int n_cols_r, n_cols_s;       // valid GEMM columns per group
+    __nv_bfloat16* out_r;
+    __nv_bfloat16* out_s;
+    int ld_r, ld_s;
+    int* status;
+};
+
+template <int BN, int STAGES>
+struct Smem {
+    static constexpr uint32_t a_bytes = BM * BK * 2;
+    static constexpr uint32_t b_bytes = BN * BK * 2;
+    static constexpr uint32_t ring = STAGES * (a_bytes + b_bytes);
+    static constexpr uint32_t bars = 8 * (2 * STAGES + 5);
+    static constexpr uint32_t tables = 4 * (3 * (kMaxRouted + 2));
+    static constexpr uint32_t total = 1024 + ring + bars + 16 + tables;
+};
+
+// Bounded wait on an mbarrier phase. Returns false if the CTA is aborting or the wait expired.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* status) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            *abort_flag = 1;
+            set_status(status, MOE_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Wait used while draining after an abort: bounded, ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int BN, int STAGES, bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcArgs args) {
+    using S = Smem<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* a_ring = base;
+    uint8_t* b_ring = base + STAGES * S::a_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + S::ring);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = bars + 2 * STAGES + 2;
+    uint64_t* drain = bars + 2 * STAGES + 4;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + S::ring + S::bars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    int* prefix = reinterpret_cast<int*>(base + S::ring + S::bars + 16);
+    int* rows_s = prefix + (kMaxRouted + 2);
+    int* row0_s = rows_s + (kMaxRouted + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const GroupTiles gt = args.gt;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(ptx::smem_addr(&tfull[a]), 1);
+            ptx::mbar_init(ptx::smem_addr(&tempty[a]), 4);
+        }
+        ptx::mbar_init(ptx::smem_addr(drain), 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&args.a_r);
+        ptx::prefetch_tmap(&args.a_s);
+        ptx::prefetch_tmap(&args.b_r);
+        ptx::prefetch_tmap(&args.b_s);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), 2 * BN);
+        ptx::tmem_relinquish();
+    }
+    build_tile_prefix<BM>(prefix, rows_s, row0_s, args.offsets, gt);   // contains __syncthreads
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int total = prefix[gt.n_groups];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, prefix, rows_s, row0_s, gt);
+                const bool sh = ti.group == 0;
+                const CUtensorMap* am = sh ? &args.a_s : &args.a_r;
+                const CUtensorMap* bm = sh ? &args.b_s : &args.b_r;
+                const int kb_n = sh ? args.k_blocks_s : args.k_blocks_r;
+                const int a_y = ti.row0 + ti.m_blk * BM;
+                const int b_y = (sh ? 0 : (ti.group - 1) * args.b_rows_per_expert) + ti.n_blk * BN;
+                for (int kb = 0; kb < kb_n; ++kb) {
+                    if (!wait_phase(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag,
+                                    args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = ptx::smem_addr(&full[stage]);
+                    ptx::mbar_arrive_expect_tx(fb, S::a_bytes + S::b_bytes);
+                    ptx::tma_load_2d(ptx::smem_addr(a_ring + stage * S::a_bytes), am, kb * BK, a_y,
+                                     fb);
+                    ptx::tma_load_2d(ptx::smem_addr(b_ring + stage * S::b_bytes), bm, kb * BK, b_y,
+                                     fb);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // let the loads already issued land before the CTA can exit
+                for (long i = 0; i < issued && i < STAGES; ++i) {
+                    if (--stage < 0) {
+                        stage = STAGES - 1;
+                        phase ^= 1;
+                    }
+                    drain_wait(ptx::smem_addr(&full[stage]), phase);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------- MMA issuer ----
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true, any = false;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile(t, prefix, rows_s, row0_s, gt);
+                const int kb_n = ti.group == 0 ? args.k_blocks_s : args.k_blocks_r;
+                if (!wait_phase(ptx::smem_addr(&tempty[acc]), acc_phase ^ 1, abort_flag,
+                                args.status))
+                    break;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * BN;
+                for (int kb = 0; kb < kb_n; ++kb) {
+                    if (!wait_phase(ptx::smem_addr(&full[stage]), phase, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a0 = ptx::smem_addr(a_ring + stage * S::a_bytes);
+                    const uint32_t b0 = ptx::smem_addr(b_ring + stage * S::b_bytes);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        ptx::mma_f16(d_tmem, ptx::sw128_kmajor_desc(a0 + k * 32),
+                                     ptx::sw128_kmajor_desc(b0 + k * 32), idesc,
+                                     (kb | k) != 0 ? 1u : 0u);
+                    any = true;
+                    ptx::mma_commit(ptx::smem_addr(&empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(ptx::smem_addr(&tfull[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            if (*abort_flag && any) {   // make sure no MMA is still writing TMEM
+                ptx::mma_commit(ptx::smem_addr(drain));
+                drain_wait(ptx::smem_addr(drain), 0);
+            }
+        }
+    } else {
+        // --------------------------------------------------------------------- epilogue ----
+        const int quarter = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const TileInfo ti = decode_tile(t, prefix, rows_s, row0_s, gt);
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_phase(ptx::smem_addr(&tfull[acc]), acc_phase, abort_flag, args.status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const bool sh = ti.group == 0;
+            const int r = ti.m_blk * BM + quarter * 32 + lane;     // row inside the group
+            const bool valid = r < ti.m_rows;
+            __nv_bfloat16* out = sh ? args.out_s : args.out_r;
+            const int ld = sh ? args.ld_s : args.ld_r;
+            const int n_cols = sh ? args.n_cols_s : args.n_cols_r;
+            const size_t orow = (size_t)(ti.row0 + r) * ld;
+            const uint32_t t_base = tmem + acc * BN + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                const int col0 = ti.n_blk * BN + c * 32;
+                if (col0 >= n_cols) break;
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(t_base + c * 32, v);
+                ptx::tmem_ld_wait();
+                if (!valid) continue;
+                if constexpr (GATEUP) {
+                    uint32_t o[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float g0 = __uint_as_float(v[2 * q]), g1 = __uint_as_float(v[2 * q + 1]);
+                        const float u0 = __uint_as_float(v[16 + 2 * q]);
+                        const float u1 = __uint_as_float(v[16 + 2 * q + 1]);
+                        o[q] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(out + orow + col0 / 2);
+                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                } else {
+                    uint32_t o[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        o[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+                    uint4* dst = reinterpret_cast<uint4*>(out + orow + col0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&tempty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 2 * BN);
+    }
+}
+
+// ------------------------------------------------------------------------- host side ----
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] as a 2D tensor map with a [box_rows x 64] box.
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn || rows == 0 || cols == 0) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool GATEUP>
+cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
+    using S = Smem<BN, STAGES>;
+    auto kern = gemm_tc_kernel<BN, STAGES, GATEUP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)S::total);
+    if (e != cudaSuccess) return e;
+    const int grid = max(1, min(sm_count(), max_tiles));
+    kern<<<grid, kThreads, S::total, st>>>(args);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+struct GemmShape {
+    const void *a_r, *a_s, *b_r, *b_s;
+    uint64_t a_rows_r, a_rows_s, k_r, k_s;     // A rows and K extents
+    uint64_t b_rows_r, b_rows_s;              // B total rows
+    int b_rows_per_expert, n_cols_r, n_cols_s;
+    void *out_r, *out_s;
+    int ld_r, ld_s;
+};
+
+template <bool GATEUP>
+cudaError_t run_gemm(const Dims& m, const GemmShape& g, const int* offsets, int* status,
+                     cudaStream_t st) {
+    const bool shared = m.Ks > 0;
+    const int bn = (g.n_cols_r % 256 == 0 && (!shared || g.n_cols_s % 256 == 0)) ? 256 : 128;
+    TcArgs a{};
+    if (!make_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, BM) ||
+        !make_map(&a.b_r, g.b_r, g.b_rows_r, g.k_r, bn))
+        return cudaErrorInvalidValue;
+    if (shared) {
+        if (!make_map(&a.a_s, g.a_s, g.a_rows_s, g.k_s, BM) ||
+            !make_map(&a.b_s, g.b_s, g.b_rows_s, g.k_s, bn))
+            return cudaErrorInvalidValue;
+    } else {
+        a.a_s = a.a_r;   // the shared group is empty and never loads
+        a.b_s = a.b_r;
+    }
+    a.offsets = offsets;
+    a.gt.n_groups = 1 + m.N;
+    a.gt.has_shared = shared;
+    a.gt.T = m.T;
+    a.gt.n_tiles_r = (g.n_cols_r + bn - 1) / bn;
+    a.gt.n_tiles_s = shared ? (g.n_cols_s + bn - 1) / bn : 0;
+    a.k_blocks_r = (int)((g.k_r + BK - 1) / BK);
+    a.k_blocks_s = shared ? (int)((g.k_s + BK - 1) / BK) : 0;
+    a.b_rows_per_expert = g.b_rows_per_expert;
+    a.n_cols_r = g.n_cols_r;
+    a.n_cols_s = g.n_cols_s;
+    a.out_r = static_cast<__nv_bfloat16*>(g.out_r);
+    a.out_s = static_cast<__nv_bfloat16*>(g.out_s);
+    a.ld_r = g.ld_r;
+    a.ld_s = g.ld_s;
+    a.status = status;
+    // upper bound of the tiles: sum over experts of ceil(M_j / 128) <= T*K'/128 + N'
+    const long routed_mblk = (long)m.T * m.K / BM + m.N;
+    const long max_tiles = routed_mblk * a.gt.n_tiles_r + (long)((m.T + BM - 1) / BM) * a.gt.n_tiles_s;
+    const int mt = (int)std::min<long>(max_tiles, 1 << 30);
+    if (bn == 256) return launch_tc<256, 4, GATEUP>(a, mt, st);
+    return launch_tc<128, 6, GATEUP>(a, mt, st);
+}
+
+}  // namespace
+
+cudaError_t launch_expert_gemms(const Dims& m, const void* u, const void* x_perm,
+                                const void* packed, const int* offsets, void* act_r, void* act_s,
+                                void* y_r, void* y_s, int* status, cudaStream_t st,
+                                cudaEvent_t mid_event) {
+    if (m.T == 0) {
+        if (mid_event) cudaEventRecord(mid_event, st);
+        return cudaSuccess;
+    }
+    if (m.dtype == MOE_DTYPE_F32)
+        return launch_expert_gemms_simt(m, u, x_perm, packed, offsets, act_r, act_s, y_r, y_s, st,
+                                        mid_event);
+    const PackLayout P = pack_layout(m);
+    const char* pk = static_cast<const char*>(packed);
+    const uint64_t TK = (uint64_t)m.T * m.K, KsI = (uint64_t)m.Ks * m.I;
+    GemmShape gu{};
+    gu.a_r = x_perm;
+    gu.a_s = u;
+    gu.b_r = pk + P.gu_r * 2;
+    gu.b_s = pk + P.gu_s * 2;
+    gu.a_rows_r = TK;
+    gu.a_rows_s = m.T;
+    gu.k_r = gu.k_s = m.d;
+    gu.b_rows_r = (uint64_t)m.N * 2 * m.I;
+    gu.b_rows_s = 2 * KsI;
+    gu.b_rows_per_expert = 2 * m.I;
+    gu.n_cols_r = 2 * m.I;
+    gu.n_cols_s = (int)(2 * KsI);
+    gu.out_r = act_r;
+    gu.out_s = act_s;
+    gu.ld_r = m.I;
+    gu.ld_s = (int)KsI;
+    cudaError_t e = run_gemm<true>(m, gu, offsets, status, st);
+    if (e != cudaSuccess) return e;
+    if (mid_event) cudaEventRecord(mid_event, st);
+    GemmShape dn{};
+    dn.a_r = act_r;
+    dn.a_s = act_s;
+    dn.b_r = pk + P.dn_r * 2;
+    dn.b_s = pk + P.dn_s * 2;
+    dn.a_rows_r = TK;
+    dn.a_rows_s = m.T;
+    dn.k_r = m.I;
+    dn.k_s = KsI;
+    dn.b_rows_r = (uint64_t)m.N * m.d;
+    dn.b_rows_s = m.d;
+    dn.b_rows_per_expert = m.d;
+    dn.n_cols_r = dn.n_cols_s = m.d;
+    dn.out_r = y_r;
+    dn.out_s = y_s;
+    dn.ld_r = dn.ld_s = m.d;
+    return run_gemm<false>(m, dn, offsets, status, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,77 @@
+// groups.cuh -- tile enumeration of the grouped expert GEMMs.
+//
+// Group 0 is the dense shared group (all T tokens, present when K_s > 0); groups 1..N' are the
+// routed experts, expert j owning rows offsets[j] .. offsets[j+1]-1 of the permuted matrices.
+// A group of M rows and Nc output columns has ceil(M/BM) * ceil(Nc/BN) tiles, enumerated with the
+// column tile fastest so that CTAs running at the same time share the group's A rows and weights
+// through L2. Tile t of the whole launch belongs to the group g with prefix[g] <= t < prefix[g+1].
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+struct GroupTiles {
+    int n_groups;      // 1 + N'
+    int has_shared;    // K_s > 0 (group 0 is empty otherwise)
+    int T;             // rows of the shared group
+    int n_tiles_r;     // column tiles of a routed group
+    int n_tiles_s;     // column tiles of the shared group
+};
+
+struct TileInfo {
+    int group;         // 0 = shared, 1 + j = routed expert j
+    int m_rows;        // rows of the group
+    int row0;          // first row of the group in its A / output matrix
+    int m_blk, n_blk;  // tile coordinates inside the group
+};
+
+// Fills prefix[0 .. n_groups] (shared memory) from offsets; every thread of the CTA must call it.
+template <int BM>
+__device__ __forceinline__ void build_tile_prefix(int* prefix, int* rows_s, int* row0_s,
+                                                  const int* __restrict__ offsets,
+                                                  const GroupTiles& gt) {
+    const int N = gt.n_groups - 1;
+    for (int j = threadIdx.x; j <= N; j += blockDim.x) {
+        if (j == 0) {
+            rows_s[0] = gt.has_shared ? gt.T : 0;
+            row0_s[0] = 0;
+        } else {
+            const int lo = offsets[j - 1], hi = offsets[j];
+            rows_s[j] = max(hi - lo, 0);
+            row0_s[j] = lo;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        prefix[0] = 0;
+        for (int g = 0; g <= N; ++g) {
+            const int nt = g == 0 ? gt.n_tiles_s : gt.n_tiles_r;
+            acc += ((rows_s[g] + BM - 1) / BM) * nt;
+            prefix[g + 1] = acc;
+        }
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const int* rows_s,
+                                                const int* row0_s, const GroupTiles& gt) {
+    int lo = 0, hi = gt.n_groups - 1;   // find g with prefix[g] <= t < prefix[g+1]
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    TileInfo ti;
+    ti.group = lo;
+    ti.m_rows = rows_s[lo];
+    ti.row0 = row0_s[lo];
+    const int nt = lo == 0 ? gt.n_tiles_s : gt.n_tiles_r;
+    const int local = t - prefix[lo];
+    ti.m_blk = local / nt;
+    ti.n_blk = local % nt;
+    return ti;
+}
+
+}  // namespace moe

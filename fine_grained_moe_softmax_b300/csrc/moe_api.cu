@@ -1,0 +1,340 @@
+// moe_api.cu -- the C ABI (include/moe_b300.h): argument validation, workspace layout, and the
+// order of kernel launches for each entry point. No device memory is allocated here; every
+// intermediate lives in the caller's workspace.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 148;
+    }
+    return cached[dev];
+}
+
+namespace {
+
+int check_cfg(const moe_config* c, Dims* m) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->T < 0 || c->d <= 0 || c->n_shared < 0 || c->n_routed <= 0 || c->inter <= 0 ||
+        c->top_k <= 0 || c->top_k > c->n_routed || c->n_groups <= 0 ||
+        c->n_groups > c->n_routed || (c->renormalize != 0 && c->renormalize != 1) ||
+        (c->dtype != MOE_DTYPE_F32 && c->dtype != MOE_DTYPE_BF16))
+        return MOE_ERR_INVALID_ARG;
+    if (c->d % 64 != 0 || c->inter % 16 != 0 || c->n_routed > kMaxRouted || c->top_k > kMaxTopK)
+        return MOE_ERR_UNSUPPORTED;
+    // row indices and element counts stay inside int32 / the tensor-map limits
+    const long long TK = (long long)c->T * c->top_k;
+    if (TK >= (1ll << 31) || (long long)c->n_shared * c->inter >= (1ll << 31) ||
+        (long long)c->n_routed * 2 * c->inter >= (1ll << 31) ||
+        (long long)c->n_routed * c->d >= (1ll << 31))
+        return MOE_ERR_UNSUPPORTED;
+    m->T = c->T;
+    m->d = c->d;
+    m->Ks = c->n_shared;
+    m->N = c->n_routed;
+    m->I = c->inter;
+    m->K = c->top_k;
+    m->renorm = c->renormalize;
+    m->D = c->n_groups;
+    m->a1 = c->alpha1;
+    m->a2 = c->alpha2;
+    m->dtype = c->dtype;
+    return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_ws(const Dims& m, const void* ws, size_t ws_bytes) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < ws_layout(m).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T> T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ------------------------------------------------------------------- stage timing ----
+
+struct Profile {
+    std::mutex mu;
+    bool on = false;
+    int max_calls = 0, recorded = 0;
+    std::vector<cudaEvent_t> ev;   // (MOE_N_STAGES + 1) per call
+};
+Profile g_prof;
+
+void free_profile_events() {
+    for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+    g_prof.ev.clear();
+    g_prof.recorded = 0;
+}
+
+// Events of the next recorded call, or null when not profiling / out of slots.
+cudaEvent_t* profile_slot() {
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (!g_prof.on || g_prof.recorded >= g_prof.max_calls) return nullptr;
+    return &g_prof.ev[(size_t)(g_prof.recorded++) * (MOE_N_STAGES + 1)];
+}
+
+struct Marks {
+    cudaEvent_t* ev;
+    cudaStream_t st;
+    void mark(int i) {
+        if (ev) cudaEventRecord(ev[i], st);
+    }
+    cudaEvent_t at(int i) { return ev ? ev[i] : nullptr; }
+};
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_config* cfg) {
+    Dims m;
+    if (check_cfg(cfg, &m) != MOE_OK) return 0;
+    return ws_layout(m).total;
+}
+
+size_t moe_packed_weight_bytes(const moe_config* cfg) {
+    Dims m;
+    if (check_cfg(cfg, &m) != MOE_OK) return 0;
+    return pack_layout(m).total * (size_t)m.elem();
+}
+
+int moe_pack_weights(const moe_config* cfg, const void* w_gate, const void* w_up,
+                     const void* w_down, void* packed, moe_stream_t stream) {
+    Dims m;
+    int rc = check_cfg(cfg, &m);
+    if (rc != MOE_OK) return rc;
+    if (!w_gate || !w_up || !w_down || !packed || !aligned16(w_gate) || !aligned16(w_up) ||
+        !aligned16(w_down) || !aligned16(packed))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_pack(m, w_gate, w_up, w_down, packed, (cudaStream_t)stream));
+}
+
+int moe_route(const moe_config* cfg, const void* u, const void* centroids,
+              const float* logit_bias, int32_t* topk_idx, float* topk_gate, int32_t* counts,
+              float* psum, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    Dims m;
+    int rc = check_cfg(cfg, &m);
+    if (rc != MOE_OK) return rc;
+    if ((m.T > 0 && (!u || !topk_idx || !topk_gate || !aligned16(u))) || !centroids ||
+        !aligned16(centroids) || !counts || !psum)
+        return MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(m, ws, ws_bytes)) != MOE_OK) return rc;
+    const WsLayout L = ws_layout(m);
+    cudaStream_t st = (cudaStream_t)stream;
+    int* status = at<int>(ws, L.status);
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaError_t e = launch_router(m, u, centroids, logit_bias, topk_idx, topk_gate,
+                                  at<int>(ws, L.tile_counts), at<float>(ws, L.tile_psum), status,
+                                  st);
+    if (e == cudaSuccess)
+        e = launch_route_reduce(m, at<int>(ws, L.tile_counts), at<float>(ws, L.tile_psum),
+                                counts, psum, st);
+    return cuda_rc(e);
+}
+
+int moe_permute(const moe_config* cfg, const int32_t* topk_idx, const int32_t* counts,
+                int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, void* ws,
+                size_t ws_bytes, moe_stream_t stream) {
+    Dims m;
+    int rc = check_cfg(cfg, &m);
+    if (rc != MOE_OK) return rc;
+    if ((m.T > 0 && (!topk_idx || !perm_token || !perm_slot)) || !offsets)
+        return MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(m, ws, ws_bytes)) != MOE_OK) return rc;
+    const WsLayout L = ws_layout(m);
+    cudaStream_t st = (cudaStream_t)stream;
+    int* status = at<int>(ws, L.status);
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    int* tc = at<int>(ws, L.tile_counts);
+    int* tb = at<int>(ws, L.tile_base);
+    cudaError_t e = launch_tile_hist(m, topk_idx, tc, status, st);
+    if (e == cudaSuccess) e = launch_perm_scan(m, tc, counts, offsets, tb, status, st);
+    if (e == cudaSuccess) e = launch_perm_scatter(m, topk_idx, tb, perm_token, perm_slot, st);
+    return cuda_rc(e);
+}
+
+int moe_expert_ffn(const moe_config* cfg, const void* u, const void* packed_w,
+                   const int32_t* offsets, const int32_t* perm_token, void* y_routed,
+                   void* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    Dims m;
+    int rc = check_cfg(cfg, &m);
+    if (rc != MOE_OK) return rc;
+    if (!packed_w || !aligned16(packed_w) || !offsets ||
+        (m.T > 0 && (!u || !aligned16(u) || !perm_token || !y_routed || !aligned16(y_routed) ||
+                     (m.Ks > 0 && (!y_shared || !aligned16(y_shared))))))
+        return MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(m, ws, ws_bytes)) != MOE_OK) return rc;
+    const WsLayout L = ws_layout(m);
+    cudaStream_t st = (cudaStream_t)stream;
+    int* status = at<int>(ws, L.status);
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaError_t e = launch_gather_rows(m, u, offsets, perm_token, at<void>(ws, L.x_perm), status,
+                                       st);
+    if (e == cudaSuccess)
+        e = launch_expert_gemms(m, u, at<void>(ws, L.x_perm), packed_w, offsets,
+                                at<void>(ws, L.act_r), at<void>(ws, L.act_s), y_routed, y_shared,
+                                status, st, nullptr);
+    return cuda_rc(e);
+}
+
+int moe_combine(const moe_config* cfg, const void* u, const void* y_routed, const void* y_shared,
+                const int32_t* perm_slot, const float* topk_gate, void* h, void* ws,
+                size_t ws_bytes, moe_stream_t stream) {
+    Dims m;
+    int rc = check_cfg(cfg, &m);
+    if (rc != MOE_OK) return rc;
+    if (m.T > 0 && (!u || !y_routed || !perm_slot || !topk_gate || !h || !aligned16(u) ||
+                    !aligned16(y_routed) || !aligned16(h) || (m.Ks > 0 && !y_shared) ||
+                    (y_shared && !aligned16(y_shared))))
+        return MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(m, ws, ws_bytes)) != MOE_OK) return rc;
+    const WsLayout L = ws_layout(m);
+    cudaStream_t st = (cudaStream_t)stream;
+    int* status = at<int>(ws, L.status);
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_rc(launch_combine(m, u, y_routed, y_shared, perm_slot, topk_gate, h, status, st));
+}
+
+int moe_balance_stats(const moe_config* cfg, const int32_t* counts, const float* psum, float* f,
+                      float* P, float* losses, moe_stream_t stream) {
+    Dims m;
+    int rc = check_cfg(cfg, &m);
+    if (rc != MOE_OK) return rc;
+    if (!counts || !psum || !f || !P || !losses) return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_balance(m, counts, psum, f, P, losses, (cudaStream_t)stream));
+}
+
+int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroids,
+                      const float* logit_bias, const void* packed_w, void* h, int32_t* topk_idx,
+                      float* topk_gate, int32_t* counts, float* f, float* P, float* losses,
+                      void* ws, size_t ws_bytes, moe_stream_t stream) {
+    Dims m;
+    int rc = check_cfg(cfg, &m);
+    if (rc != MOE_OK) return rc;
+    if ((m.T > 0 && (!u || !h || !topk_idx || !topk_gate || !aligned16(u) || !aligned16(h))) ||
+        !centroids || !aligned16(centroids) || !packed_w || !aligned16(packed_w) || !counts ||
+        !f || !P || !losses)
+        return MOE_ERR_INVALID_ARG;
+    if ((rc = check_ws(m, ws, ws_bytes)) != MOE_OK) return rc;
+    const WsLayout L = ws_layout(m);
+    cudaStream_t st = (cudaStream_t)stream;
+    int* status = at<int>(ws, L.status);
+    int* tc = at<int>(ws, L.tile_counts);
+    float* tp = at<float>(ws, L.tile_psum);
+    int* tb = at<int>(ws, L.tile_base);
+    float* psum = at<float>(ws, L.psum);
+    int* offsets = at<int>(ws, L.offsets);
+    int* perm_token = at<int>(ws, L.perm_token);
+    int* perm_slot = at<int>(ws, L.perm_slot);
+    Marks mk{profile_slot(), st};
+
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    mk.mark(0);
+    cudaError_t e = launch_router(m, u, centroids, logit_bias, topk_idx, topk_gate, tc, tp, status,
+                                  st);
+    if (e == cudaSuccess) e = launch_route_reduce(m, tc, tp, counts, psum, st);
+    mk.mark(1);
+    if (e == cudaSuccess) e = launch_perm_scan(m, tc, nullptr, offsets, tb, status, st);
+    if (e == cudaSuccess) e = launch_perm_scatter(m, topk_idx, tb, perm_token, perm_slot, st);
+    mk.mark(2);
+    if (e == cudaSuccess) e = launch_gather(m, u, perm_slot, at<void>(ws, L.x_perm), status, st);
+    mk.mark(3);
+    if (e == cudaSuccess)
+        e = launch_expert_gemms(m, u, at<void>(ws, L.x_perm), packed_w, offsets,
+                                at<void>(ws, L.act_r), at<void>(ws, L.act_s), at<void>(ws, L.y_r),
+                                at<void>(ws, L.y_s), status, st, mk.at(4));
+    mk.mark(5);
+    if (e == cudaSuccess)
+        e = launch_combine(m, u, at<void>(ws, L.y_r), at<void>(ws, L.y_s), perm_slot, topk_gate, h,
+                           status, st);
+    mk.mark(6);
+    if (e == cudaSuccess) e = launch_balance(m, counts, psum, f, P, losses, st);
+    mk.mark(7);
+    return cuda_rc(e);
+}
+
+int moe_device_status(const void* ws, moe_stream_t stream) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return v;
+}
+
+const char* moe_status_string(int s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_CORRUPT_INPUT: return "MOE_ERR_CORRUPT_INPUT";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+int moe_profile_enable(int enable, int max_calls) {
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    free_profile_events();
+    g_prof.on = false;
+    if (!enable) return MOE_OK;
+    if (max_calls <= 0) return MOE_ERR_INVALID_ARG;
+    g_prof.ev.resize((size_t)max_calls * (MOE_N_STAGES + 1));
+    for (auto& e : g_prof.ev)
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            e = nullptr;
+            free_profile_events();
+            return MOE_ERR_CUDA;
+        }
+    g_prof.max_calls = max_calls;
+    g_prof.on = true;
+    return MOE_OK;
+}
+
+int moe_profile_read(float* ms, int* n_calls) {
+    if (!ms || !n_calls) return MOE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    for (int s = 0; s < MOE_N_STAGES; ++s) ms[s] = 0.f;
+    for (int c = 0; c < g_prof.recorded; ++c) {
+        cudaEvent_t* ev = &g_prof.ev[(size_t)c * (MOE_N_STAGES + 1)];
+        if (cudaEventSynchronize(ev[MOE_N_STAGES]) != cudaSuccess) return MOE_ERR_CUDA;
+        for (int s = 0; s < MOE_N_STAGES; ++s) {
+            float t = 0.f;
+            if (cudaEventElapsedTime(&t, ev[s], ev[s + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+            ms[s] += t;
+        }
+    }
+    *n_calls = g_prof.recorded;
+    return MOE_OK;
+}
+
+}  // extern "C"

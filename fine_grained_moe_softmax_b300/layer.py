@@ -1,0 +1,69 @@
+"""Device-resident MoE layer: packed weights, workspace and outputs for repeated forward calls.
+
+PyTorch only provides the device memory and the stream here; the forward pass itself is one call
+of the C ABI's ``moe_layer_forward``.
+"""
+from __future__ import annotations
+
+import copy
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class MoELayer:
+    """Holds one layer's weights in the library's packed layout plus a workspace sized for up to
+    ``cfg.T`` tokens per call.
+
+    centroids [N', d], w_gate / w_up [K_s + N', I, d], w_down [K_s + N', d, I] (shared experts
+    first), logit_bias [N'] fp32 or None; all in the config's dtype (bias fp32).
+    """
+
+    def __init__(self, cfg: B.MoEConfig, centroids, w_gate, w_up, w_down, logit_bias=None,
+                 device="cuda", stream=None):
+        self.cfg = copy.copy(cfg)
+        self.device = torch.device(device)
+        dt = cfg.torch_dtype()
+        dev = self.device
+        self.centroids = centroids.to(dev, dt).contiguous()
+        self.logit_bias = None if logit_bias is None else logit_bias.to(dev, torch.float32).contiguous()
+        self.packed = torch.empty(B.moe_packed_weight_bytes(self.cfg), dtype=torch.uint8,
+                                  device=dev)
+        w_gate = w_gate.to(dev, dt).contiguous()
+        w_up = w_up.to(dev, dt).contiguous()
+        w_down = w_down.to(dev, dt).contiguous()
+        B.moe_pack_weights(self.cfg, w_gate, w_up, w_down, self.packed, stream)
+        torch.cuda.current_stream(dev).synchronize() if stream is None else stream.synchronize()
+        del w_gate, w_up, w_down
+        self.ws = torch.empty(max(B.moe_workspace_bytes(self.cfg), 256), dtype=torch.uint8,
+                              device=dev)
+        T, K, N = cfg.T, cfg.top_k, cfg.n_routed
+        self.h = torch.empty(T, cfg.d, dtype=dt, device=dev)
+        self.topk_idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+        self.topk_gate = torch.empty(T, K, dtype=torch.float32, device=dev)
+        self.counts = torch.empty(N, dtype=torch.int32, device=dev)
+        self.f = torch.empty(N, dtype=torch.float32, device=dev)
+        self.P = torch.empty(N, dtype=torch.float32, device=dev)
+        self.losses = torch.empty(2, dtype=torch.float32, device=dev)
+
+    def cfg_for(self, T: int) -> B.MoEConfig:
+        if T > self.cfg.T:
+            raise ValueError(f"{T} tokens exceed the {self.cfg.T} this layer was sized for")
+        c = copy.copy(self.cfg)
+        c.T = T
+        return c
+
+    def forward(self, u: torch.Tensor, h: Optional[torch.Tensor] = None, stream=None):
+        """Runs the layer on u [T, d]; returns h (written into ``self.h[:T]`` unless given)."""
+        T = u.shape[0]
+        cfg = self.cfg_for(T)
+        out = self.h[:T] if h is None else h
+        B.moe_layer_forward(cfg, u, self.centroids, self.logit_bias, self.packed, out,
+                            self.topk_idx[:T], self.topk_gate[:T], self.counts, self.f, self.P,
+                            self.losses, self.ws, stream)
+        return out
+
+    def device_status(self, stream=None) -> int:
+        return B.moe_device_status(self.ws, stream)

@@ -1,0 +1,171 @@
+/*
+ * moe_b300.h -- C ABI of the B300 (sm_103a) DeepSeekMoE layer-forward library.
+ *
+ * The layer: h_t = u_t + sum_{s < K_s} FFN_s(u_t) + sum_{k < K'} g_{t,k} FFN_{K_s + r_{t,k}}(u_t),
+ * over K_s always-active shared experts and N' fine-grained routed experts, each a SwiGLU FFN of
+ * intermediate width I. Routed expert r_{t,k} is the k-th best by affinity
+ * s_{t,j} = softmax_j(u_t . e_j + b_j) over the N' routed experts.
+ *
+ * Page citations:
+ *   [P1] "DeepSeekMoE 论文解读" (xxmr.cn news 118388): §两大核心策略 (fine-grained segmentation,
+ *        shared-expert isolation), §方法细节：公式与负载均衡设计 (layer formula, Topk gates,
+ *        expert- and device-level balance losses).
+ *   [P2] "【论文总结】MoE" (mickeyding.github.io): §2.2 (centroids e_i), §2.3 (f_i, P_i, T, N',
+ *        K'), §2.4 (f'_i, P'_i per device group).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensor pointers are DEVICE pointers to contiguous row-major arrays owned by the caller. The
+ *     library never allocates or frees device memory; scratch lives in the caller's workspace
+ *     `ws` of at least moe_workspace_bytes() bytes (256-byte aligned).
+ *   - Element type of u, h, centroids and expert weights: cfg->dtype (fp32 or bf16). Gates,
+ *     logit bias, affinity sums and statistics are fp32; indices and counts are int32.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     The return value reports argument and launch errors only. Errors found on the device
+ *     (a bounded wait that ran out, corrupt routing input) are written to a status word inside
+ *     `ws`; each call clears that word when it starts, and moe_device_status() reads it.
+ *   - Supported shapes: T >= 0, d % 64 == 0, I % 16 == 0, 1 <= top_k <= min(N', 16),
+ *     1 <= N' <= 256, 0 <= K_s, 1 <= n_groups <= N'. Anything else returns
+ *     MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED; there is no fallback path.
+ *   - Calls on different streams with disjoint workspaces and outputs are independent.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,   /* null pointer, negative size, top_k > N', ... */
+    MOE_ERR_UNSUPPORTED = -2,   /* valid but outside the shapes this build handles */
+    MOE_ERR_WORKSPACE = -3,     /* ws_bytes < moe_workspace_bytes(cfg) or misaligned ws */
+    MOE_ERR_CUDA = -4,          /* a CUDA runtime/driver call failed (launch, tensor map) */
+    MOE_ERR_TIMEOUT = -5,       /* device side: a bounded wait gave up (kernel returned early) */
+    MOE_ERR_CORRUPT_INPUT = -6  /* device side: routing input out of range or inconsistent */
+} moe_status;
+
+typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+typedef struct {
+    int32_t T;           /* tokens in this call */
+    int32_t d;           /* model width */
+    int32_t n_shared;    /* K_s, always-active shared experts (global ids 0..K_s-1) */
+    int32_t n_routed;    /* N', routed experts (local id j, global id K_s + j) */
+    int32_t inter;       /* I, intermediate width of every expert */
+    int32_t top_k;       /* K', routed experts chosen per token */
+    int32_t renormalize; /* 0: g = s;  1: g = s / sum over the chosen K' of s */
+    int32_t n_groups;    /* D, contiguous routed-expert groups for the device-level statistic */
+    float alpha1;        /* expert-level balance factor */
+    float alpha2;        /* device-level balance factor */
+    int32_t dtype;       /* moe_dtype of u, h, centroids and weights */
+} moe_config;
+
+/* Bytes of scratch any entry point may use for this configuration (the same figure for all). */
+size_t moe_workspace_bytes(const moe_config* cfg);
+
+/* Bytes of the packed expert-weight buffer written by moe_pack_weights. */
+size_t moe_packed_weight_bytes(const moe_config* cfg);
+
+/* Repacks caller weights into the library layout used by moe_expert_ffn / moe_layer_forward.
+ *   w_gate, w_up [K_s + N', I, d]; w_down [K_s + N', d, I] (shared experts first).
+ *   packed: device buffer of moe_packed_weight_bytes(cfg) bytes, written by this call.
+ * One kernel launch; the caller keeps ownership of all buffers. [P1 §两大核心策略: mN experts of
+ * width 1/m, K_s of them shared; the shared experts are packed as one expert of width K_s*I, which
+ * computes the same sum since their gates are all 1.] */
+int moe_pack_weights(const moe_config* cfg, const void* w_gate, const void* w_up,
+                     const void* w_down, void* packed, moe_stream_t stream);
+
+/* Router. For every token t: z_{t,j} = u_t . e_j + b_j (fp32 accumulation), s = softmax_j(z)
+ * over the N' routed experts, the K' experts of largest s (lower index first on equal s) in rank
+ * order, and their gates (s, or renormalised over the chosen K').
+ *   u [T, d]; centroids [N', d]; logit_bias [N'] fp32 or NULL (treated as 0).
+ *   topk_idx [T, K'] int32 routed ids in rank order; topk_gate [T, K'] fp32;
+ *   counts [N'] int32: tokens that chose expert j; psum [N'] fp32: sum over t of s_{t,j}.
+ * counts and psum are overwritten (not accumulated) and summed in a fixed order, so the call is
+ * deterministic. [P2 §2.2: centroid affinity; P1 §方法细节: gates from Topk over s; P2 §2.3:
+ * selection counts and mean affinity feed f_i and P_i] */
+int moe_route(const moe_config* cfg, const void* u, const void* centroids,
+              const float* logit_bias, int32_t* topk_idx, float* topk_gate, int32_t* counts,
+              float* psum, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Dispatch permutation: a stable counting sort of the T*K' (token, slot) assignments by routed
+ * expert, tokens ascending inside an expert.
+ *   topk_idx [T, K'], counts [N'] (as produced by moe_route).
+ *   offsets [N'+1]: expert j owns rows offsets[j] .. offsets[j+1]-1, offsets[N'] = T*K';
+ *   perm_token [T*K']: token of each row; perm_slot [T*K']: row of assignment (t, k) at t*K'+k.
+ * Expert ids outside [0, N') are skipped and counts that disagree with topk_idx are ignored in
+ * favour of topk_idx; both set MOE_ERR_CORRUPT_INPUT in the status word. [Sparse activation of
+ * the chosen experts, P1 §方法细节] */
+int moe_permute(const moe_config* cfg, const int32_t* topk_idx, const int32_t* counts,
+                int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, void* ws,
+                size_t ws_bytes, moe_stream_t stream);
+
+/* Expert FFNs. Routed row r (expert j with offsets[j] <= r < offsets[j+1], token perm_token[r])
+ * gets y_routed[r] = FFN_{K_s+j}(u_{perm_token[r]}); every token gets
+ * y_shared[t] = sum_{s<K_s} FFN_s(u_t) (left untouched when K_s = 0).
+ * FFN(x) = W_down (silu(W_gate x) * (W_up x)); bf16 inputs use tensor cores with fp32
+ * accumulation and round the intermediate activation and the outputs to bf16.
+ *   packed_w from moe_pack_weights; y_routed [T*K', d]; y_shared [T, d] (dtype of u).
+ * [P1 §方法细节: FFN_i; P1 §两大核心策略: shared experts always active] */
+int moe_expert_ffn(const moe_config* cfg, const void* u, const void* packed_w,
+                   const int32_t* offsets, const int32_t* perm_token, void* y_routed,
+                   void* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Gated combine with the residual, accumulated in fp32 in the fixed order u, shared, k = 0..K'-1:
+ * h_t = u_t + y_shared[t] + sum_k topk_gate[t,k] * y_routed[perm_slot[t*K'+k]].
+ * Rows outside [0, T*K') are skipped and set MOE_ERR_CORRUPT_INPUT.
+ * [P1 §方法细节: h_t = sum_i g_{i,t} FFN_i(u_t) + u_t] */
+int moe_combine(const moe_config* cfg, const void* u, const void* y_routed, const void* y_shared,
+                const int32_t* perm_slot, const float* topk_gate, void* h, void* ws,
+                size_t ws_bytes, moe_stream_t stream);
+
+/* Balance statistics (fp32): f_j = N'/(K' T) counts_j, P_j = psum_j / T,
+ * losses[0] = L_ExpBal = alpha1 sum_j f_j P_j,
+ * losses[1] = L_DevBal = alpha2 sum_g f'_g P'_g with f'_g the mean of f and P'_g the sum of P over
+ * contiguous group g (the first N' mod D groups hold one extra expert).
+ *   counts [N'] int32, psum [N'] fp32 -> f [N'], P [N'], losses [2].
+ * [P1 §方法细节: L_ExpBal, L_DevBal; P2 §2.3, §2.4] */
+int moe_balance_stats(const moe_config* cfg, const int32_t* counts, const float* psum, float* f,
+                      float* P, float* losses, moe_stream_t stream);
+
+/* The whole layer in one call: route, permute, expert FFNs, combine and statistics.
+ *   u [T, d]; centroids [N', d]; logit_bias [N'] or NULL; packed_w from moe_pack_weights;
+ *   h [T, d] out; topk_idx [T, K'], topk_gate [T, K'], counts [N'], f [N'], P [N'],
+ *   losses [2] out. Intermediates live in ws. [P1 §方法细节] */
+int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroids,
+                      const float* logit_bias, const void* packed_w, void* h, int32_t* topk_idx,
+                      float* topk_gate, int32_t* counts, float* f, float* P, float* losses,
+                      void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Waits for `stream`, then returns the device status word of `ws` (MOE_OK or a negative
+ * moe_status), or MOE_ERR_CUDA if the wait itself failed. */
+int moe_device_status(const void* ws, moe_stream_t stream);
+
+/* Human-readable name of a moe_status value (static string). */
+const char* moe_status_string(int status);
+
+/* ---- instrumentation (no effect on results) ---- */
+
+/* Kernels this library has launched in this process since load (all entry points). */
+uint64_t moe_launch_count(void);
+
+/* Per-stage timing of moe_layer_forward. enable != 0 starts recording a CUDA event around each
+ * stage (router, permute, gather, gate/up GEMM, down GEMM, combine, statistics) of the next
+ * calls, up to max_calls of them; enable == 0 stops and frees the events. */
+int moe_profile_enable(int enable, int max_calls);
+
+/* Waits for the recorded events and writes, per stage, the summed milliseconds over the recorded
+ * calls into ms[0 .. MOE_N_STAGES-1]; *n_calls receives the number of calls recorded. */
+#define MOE_N_STAGES 7
+int moe_profile_read(float* ms, int* n_calls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

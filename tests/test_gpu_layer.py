@@ -1,0 +1,148 @@
+"""GPU parity of the whole layer (moe_layer_forward through the C ABI) against the fp64 oracle.
+
+Small token counts span several 128-row tiles plus a ragged tail and are checked on every token;
+the full-size workloads are checked on all routing decisions and on a seeded sample of h rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+import oracle
+from oracle import OracleCfg
+from parity import NEAR_TIE, TOL, check_routing, rel_l2, run_layer, to_np
+
+pytestmark = pytest.mark.gpu
+
+C = moe_inputs.CONFIGS
+
+
+def _compare_layer(shape, inputs, layer, u_dev, tokens=None):
+    T = inputs["u"].shape[0]
+    cfg = OracleCfg.from_shape(shape, T=T)
+    ref_route = oracle.route(cfg, inputs["u"], inputs["centroids"], inputs.get("bias"))
+    idx = to_np(layer.topk_idx[:T])
+    gate = to_np(layer.topk_gate[:T])
+    counts = to_np(layer.counts)
+    ok = check_routing(cfg, ref_route, idx, gate, counts)
+    # statistics: the oracle's balance statistics of the GPU's own counts and the oracle's psum
+    st = oracle.balance_stats(cfg, counts, ref_route["psum"])
+    np.testing.assert_allclose(to_np(layer.f), st["f"], rtol=1e-6)
+    np.testing.assert_allclose(to_np(layer.P), st["P"], rtol=2e-4, atol=1e-7)
+    np.testing.assert_allclose(to_np(layer.losses), st["losses"], rtol=2e-4)
+    # h on the chosen tokens that are not near-ties
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    toks = toks[ok[toks]]
+    fw = oracle.forward_tokens(cfg, inputs, toks)
+    h = to_np(layer.h[:T])[toks]
+    u = to_np(u_dev)[toks]
+    tol = TOL[shape.dtype]
+    err_h = rel_l2(h, fw["h"])
+    err_moe = rel_l2(h - u, fw["h"] - u)
+    assert err_h <= tol, f"rel-L2(h) = {err_h}"
+    assert err_moe <= tol, f"rel-L2(h - u) = {err_moe}"
+    assert layer.device_status() == 0
+    return err_h, err_moe
+
+
+@pytest.mark.parametrize("name,T", [("tiny_f32", None), ("tiny_f32", 129), ("2b_bf16", 300),
+                                    ("16b_bf16", 257), ("16b_decode_bf16", None),
+                                    ("145b_zipf_bf16", 130)])
+def test_layer_all_tokens(name, T):
+    shape = C[name]
+    inputs = moe_inputs.make_inputs(shape, T=T)
+    layer, u = run_layer(shape, inputs, T=inputs["u"].shape[0])
+    _compare_layer(shape, inputs, layer, u)
+
+
+@pytest.mark.parametrize("name", ["2b_bf16", "16b_bf16", "145b_zipf_bf16"])
+def test_layer_full_size_sampled(name):
+    """Full token count in the launch configuration the benchmark times; every routing decision
+    is compared, h on a seeded sample of tokens (including the first and last tile)."""
+    shape = C[name]
+    inputs = moe_inputs.make_inputs(shape)
+    layer, u = run_layer(shape, inputs)
+    rng = np.random.default_rng(7)
+    T = shape.T
+    sample = np.unique(np.concatenate([[0, 1, 127, 128, T - 1],
+                                       rng.choice(T, 40, replace=False)]))
+    _compare_layer(shape, inputs, layer, u, tokens=sample)
+
+
+def _custom(**kw):
+    base = dict(name="custom", T=200, d=128, n_shared=1, n_routed=16, inter=32, top_k=4,
+                n_groups=4, dtype="bf16", seed=11)
+    base.update(kw)
+    return moe_inputs.MoEShape(**base)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),                                         # baseline small bf16
+    dict(renormalize=1),                            # renormalised gates
+    dict(n_shared=0),                               # no shared experts (coarse top-k special case)
+    dict(n_shared=3, inter=48),                     # several shared experts, I not a multiple of 64
+    dict(top_k=16, n_routed=16),                    # K' = N': dense softmax mixture
+    dict(top_k=1),                                  # top-1
+    dict(T=1), dict(T=127), dict(T=128), dict(T=129),
+    dict(d=64, inter=16),                           # smallest supported widths
+    dict(n_routed=256, top_k=8, n_groups=8, T=300), # widest router
+    dict(dtype="f32", renormalize=1, n_shared=2),
+    dict(dtype="f32", top_k=16, n_routed=16, T=77),
+])
+def test_layer_edge_shapes(kw):
+    shape = _custom(**kw)
+    inputs = moe_inputs.make_inputs(shape)
+    layer, u = run_layer(shape, inputs)
+    _compare_layer(shape, inputs, layer, u)
+
+
+def test_all_tokens_to_one_expert():
+    """A large logit bias sends every token to experts 5 and 9: those two routed groups hold all
+    T rows each (several row tiles), the others none. The biases keep the affinity gaps between
+    ranks 1, 2 and 3 well above the near-tie threshold."""
+    shape = _custom(T=300, top_k=2)
+    inputs = moe_inputs.make_inputs(shape)
+    bias = torch.zeros(shape.n_routed)
+    bias[5] = 16.0
+    bias[9] = 8.0
+    inputs["bias"] = bias
+    layer, u = run_layer(shape, inputs)
+    counts = to_np(layer.counts)
+    assert counts[5] == shape.T and counts[9] == shape.T and counts.sum() == 2 * shape.T
+    _compare_layer(shape, inputs, layer, u)
+
+
+def test_zero_tokens():
+    shape = _custom(T=16)
+    inputs = moe_inputs.make_inputs(shape)
+    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer
+    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
+                     inputs["w_up"], inputs["w_down"])
+    layer.counts.fill_(7)
+    layer.losses.fill_(7)
+    layer.forward(torch.empty(0, shape.d, dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert to_np(layer.counts).sum() == 0
+    assert np.all(to_np(layer.losses) == 0)
+    assert layer.device_status() == 0
+
+
+def test_deterministic():
+    shape = C["2b_bf16"]
+    inputs = moe_inputs.make_inputs(shape, T=1000)
+    layer, u = run_layer(shape, inputs, T=1000)
+    h1 = layer.h.clone()
+    p1 = layer.P.clone()
+    layer.forward(u)
+    torch.cuda.synchronize()
+    assert torch.equal(h1, layer.h)
+    assert torch.equal(p1, layer.P)
+
+
+def test_near_tie_threshold_is_rare():
+    """The exclusion rule only removes a handful of tokens at the largest workload."""
+    shape = C["16b_bf16"]
+    cfg = OracleCfg.from_shape(shape, T=4096)
+    inputs = moe_inputs.make_inputs(shape, T=4096)
+    r = oracle.route(cfg, inputs["u"], inputs["centroids"])
+    assert (r["margin"] < NEAR_TIE).sum() <= 8
