@@ -61,6 +61,7 @@ _SIG = {
                                          ctypes.c_size_t, _P]),
     "moe_device_status": (ctypes.c_int, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_selftest_bounded_wait": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint64, _P]),
     "moe_launch_count": (ctypes.c_uint64, []),
     "moe_profile_enable": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "moe_profile_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
@@ -177,6 +178,11 @@ def moe_device_status(ws, stream=None) -> int:
 
 def moe_status_string(status: int) -> str:
     return status_string(status)
+
+
+def moe_selftest_bounded_wait(ws, timeout_ns: int, stream=None):
+    _check(lib().moe_selftest_bounded_wait(_ptr(ws), _nbytes(ws), int(timeout_ns),
+                                           _stream(stream)), "moe_selftest_bounded_wait")
 
 
 def moe_launch_count() -> int:

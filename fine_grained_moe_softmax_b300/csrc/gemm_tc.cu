@@ -25,6 +25,7 @@
 #include "groups.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
+#include "waits.cuh"
 
 namespace moe {
 
@@ -38,7 +39,6 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle row
 constexpr int kThreads = 192;
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 
 struct TcArgs {
     CUtensorMap a_r, a_s, b_r, b_s;
@@ -62,31 +62,6 @@ struct Smem {
     static constexpr uint32_t tables = 4 * (3 * (kMaxRouted + 2));
     static constexpr uint32_t total = 1024 + ring + bars + 16 + tables;
 };
-
-// Bounded wait on an mbarrier phase. Returns false if the CTA is aborting or the wait expired.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           int* status) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            *abort_flag = 1;
-            set_status(status, MOE_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-// Wait used while draining after an abort: bounded, ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!ptx::mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return;
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);

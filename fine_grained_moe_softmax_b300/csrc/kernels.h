@@ -56,6 +56,9 @@ cudaError_t launch_combine(const Dims& m, const void* u, const void* y_r, const 
 cudaError_t launch_balance(const Dims& m, const int* counts, const float* psum, float* f,
                           float* P, float* losses, cudaStream_t st);
 
+// One thread waits on an mbarrier nothing arrives on; records MOE_ERR_TIMEOUT after timeout_ns.
+cudaError_t launch_bounded_wait_probe(int* status, uint64_t timeout_ns, cudaStream_t st);
+
 // Weight packing (see PackLayout).
 cudaError_t launch_pack(const Dims& m, const void* w_gate, const void* w_up, const void* w_down,
                         void* packed, cudaStream_t st);

@@ -300,6 +300,18 @@ const char* moe_status_string(int s) {
     }
 }
 
+int moe_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t timeout_ns,
+                              moe_stream_t stream) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < 256)
+        return MOE_ERR_WORKSPACE;
+    const uint64_t t = timeout_ns < 1000000ull ? 1000000ull
+                       : (timeout_ns > 2000000000ull ? 2000000000ull : timeout_ns);
+    cudaStream_t st = (cudaStream_t)stream;
+    int* status = static_cast<int*>(ws);
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_rc(launch_bounded_wait_probe(status, t, st));
+}
+
 uint64_t moe_launch_count(void) { return g_launches.load(); }
 
 int moe_profile_enable(int enable, int max_calls) {

@@ -150,6 +150,16 @@ int moe_device_status(const void* ws, moe_stream_t stream);
 /* Human-readable name of a moe_status value (static string). */
 const char* moe_status_string(int status);
 
+/* ---- failure detection ---- */
+
+/* Self-test of the bounded waits that every pipelined kernel of this library uses: launches one
+ * thread that waits on an mbarrier nothing ever arrives on. The wait gives up after timeout_ns
+ * (clamped to [1 ms, 2 s]), writes MOE_ERR_TIMEOUT to the status word of ws and the kernel returns,
+ * leaving the CUDA context usable. ws: at least 256 bytes, 256-byte aligned. Read the outcome with
+ * moe_device_status(). No page describes this; it checks the library's own failure handling. */
+int moe_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t timeout_ns,
+                              moe_stream_t stream);
+
 /* ---- instrumentation (no effect on results) ---- */
 
 /* Kernels this library has launched in this process since load (all entry points). */

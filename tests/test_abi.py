@@ -14,7 +14,7 @@ from fine_grained_moe_softmax_b300 import build as build_mod  # noqa: E402
 EXPECTED = {"moe_workspace_bytes", "moe_packed_weight_bytes", "moe_pack_weights", "moe_route",
             "moe_permute", "moe_expert_ffn", "moe_combine", "moe_balance_stats",
             "moe_layer_forward", "moe_device_status", "moe_status_string", "moe_launch_count",
-            "moe_profile_enable", "moe_profile_read"}
+            "moe_profile_enable", "moe_profile_read", "moe_selftest_bounded_wait"}
 
 
 @pytest.fixture(scope="module")
@@ -97,6 +97,8 @@ def test_null_and_workspace_errors(lib):
     assert lib.moe_pack_weights(ctypes.byref(cfg), fake, None, fake, fake, None) == -1
     assert lib.moe_device_status(None, None) == -1
     assert lib.moe_profile_enable(1, 0) == -1
+    assert lib.moe_selftest_bounded_wait(None, 256, 1000, None) == -3
+    assert lib.moe_selftest_bounded_wait(P((1 << 20) + 8), 256, 1000, None) == -3
 
 
 def test_profile_read_without_calls(lib):
