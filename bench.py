@@ -53,6 +53,22 @@ def load_peaks():
     return 6400.0, 1800.0, 1400.0, "fallback"
 
 
+def rank_token_seed(sh, rank: int) -> int:
+    """Each rank draws its own token batch; the expert weights are the same on every rank."""
+    return sh.seed + 7919 * rank
+
+
+def max_over_ranks(values, world: int, device=None):
+    """Element-wise maximum over the ranks of the default process group (identity for 1 rank)."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 # ------------------------------------------------------------------------------ clocks ----
 
 class ClockSampler:
@@ -172,7 +188,7 @@ def run_ours(args, sh, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     T = sh.T
-    inputs = moe_inputs.make_inputs(sh, seed=sh.seed + 7919 * rank)
+    inputs = moe_inputs.make_inputs(sh, seed=rank_token_seed(sh, rank))
     cfg = moe.MoEConfig.from_shape(sh)
     layer = moe.MoELayer(cfg, inputs["centroids"], inputs["w_gate"], inputs["w_up"],
                          inputs["w_down"], inputs["bias"], device=dev)
@@ -246,11 +262,7 @@ def run_ours(args, sh, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device status {moe.moe_status_string(status)} after timing")
 
-    # max over ranks
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = t.tolist()
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], world, dev)
     if rank != 0:
         return
 
@@ -307,10 +319,14 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=512)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (small profiling captures only; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     sh = moe_inputs.CONFIGS[args.config]
+    if args.tokens is not None:
+        sh = sh.with_(T=args.tokens, name=f"{sh.name}_T{args.tokens}")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

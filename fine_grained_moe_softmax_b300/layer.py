@@ -35,7 +35,10 @@ class MoELayer:
         w_up = w_up.to(dev, dt).contiguous()
         w_down = w_down.to(dev, dt).contiguous()
         B.moe_pack_weights(self.cfg, w_gate, w_up, w_down, self.packed, stream)
-        torch.cuda.current_stream(dev).synchronize() if stream is None else stream.synchronize()
+        if stream is None:
+            torch.cuda.current_stream(dev).synchronize()
+        else:
+            stream.synchronize()
         del w_gate, w_up, w_down
         self.ws = torch.empty(max(B.moe_workspace_bytes(self.cfg), 256), dtype=torch.uint8,
                               device=dev)
@@ -67,3 +70,33 @@ class MoELayer:
 
     def device_status(self, stream=None) -> int:
         return B.moe_device_status(self.ws, stream)
+
+    def global_balance_stats(self, T_local: int, group=None, stream=None):
+        """Balance statistics over the tokens of every rank in ``group``: the per-rank counts and
+        affinity sums (2N' values) are summed across ranks, then moe_balance_stats runs with the
+        global token count. Returns (f, P, losses) device tensors. Only needed when the token
+        batch is split across GPUs; a single GPU's forward already fills f, P and losses.
+        The local affinity sums are recovered as P * T_local (within an fp32 rounding)."""
+        counts = self.counts.clone()
+        psum = self.P * float(T_local)
+        T_total = allreduce_routing_stats(counts, psum, T_local, group)
+        cfg = copy.copy(self.cfg)
+        cfg.T = T_total
+        f = torch.empty_like(self.f)
+        P = torch.empty_like(self.P)
+        losses = torch.empty_like(self.losses)
+        B.moe_balance_stats(cfg, counts, psum, f, P, losses, stream)
+        return f, P, losses
+
+
+def allreduce_routing_stats(counts: torch.Tensor, psum: torch.Tensor, T_local: int,
+                            group=None) -> int:
+    """Sums per-expert selection counts (int32) and affinity sums (fp32) over the ranks of
+    ``group`` in place and returns the total token count. Works on CPU tensors with gloo and on
+    CUDA tensors with NCCL."""
+    import torch.distributed as dist
+    dist.all_reduce(counts, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(psum, op=dist.ReduceOp.SUM, group=group)
+    t = torch.tensor([int(T_local)], dtype=torch.int64, device=counts.device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return int(t.item())
