@@ -29,6 +29,36 @@
 
 namespace moe {
 
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] as a 2D tensor map with a [box_rows x 64] box, 128-byte
+// swizzle, zero fill outside the matrix.
+bool encode_bf16_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                     int box_rows) {
+    auto fn = encode_fn();
+    if (!fn || rows == 0 || cols == 0) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 cudaError_t launch_expert_gemms_simt(const Dims& m, const void* u, const void* x_perm,
                                      const void* packed, const int* offsets, void* act_r,
                                      void* act_s, void* y_r, void* y_s, cudaStream_t st,
@@ -285,34 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
 // ------------------------------------------------------------------------- host side ----
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// Row-major bf16 matrix [rows, cols] as a 2D tensor map with a [box_rows x 64] box.
-bool make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, int box_rows) {
-    auto fn = encode_fn();
-    if (!fn || rows == 0 || cols == 0) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
 template <int BN, int STAGES, bool GATEUP>
 cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
     using S = Smem<BN, STAGES>;
@@ -341,12 +343,12 @@ cudaError_t run_gemm(const Dims& m, const GemmShape& g, const int* offsets, int*
     const bool shared = m.Ks > 0;
     const int bn = (g.n_cols_r % 256 == 0 && (!shared || g.n_cols_s % 256 == 0)) ? 256 : 128;
     TcArgs a{};
-    if (!make_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, BM) ||
-        !make_map(&a.b_r, g.b_r, g.b_rows_r, g.k_r, bn))
+    if (!encode_bf16_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, BM) ||
+        !encode_bf16_map(&a.b_r, g.b_r, g.b_rows_r, g.k_r, bn))
         return cudaErrorInvalidValue;
     if (shared) {
-        if (!make_map(&a.a_s, g.a_s, g.a_rows_s, g.k_s, BM) ||
-            !make_map(&a.b_s, g.b_s, g.b_rows_s, g.k_s, bn))
+        if (!encode_bf16_map(&a.a_s, g.a_s, g.a_rows_s, g.k_s, BM) ||
+            !encode_bf16_map(&a.b_s, g.b_s, g.b_rows_s, g.k_s, bn))
             return cudaErrorInvalidValue;
     } else {
         a.a_s = a.a_r;   // the shared group is empty and never loads

@@ -3,6 +3,7 @@
 // counter by the number of kernels it launched.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -14,22 +15,41 @@ cudaError_t launch_router(const Dims& m, const void* u, const void* centroids, c
                           int* topk_idx, float* topk_gate, int* tile_counts, float* tile_psum,
                           int* status, cudaStream_t st);
 
-// Sums the per-tile histograms and affinity sums in tile order into counts [N] and psum [N].
-cudaError_t launch_route_reduce(const Dims& m, const int* tile_counts, const float* tile_psum,
-                                int* counts, float* psum, cudaStream_t st);
+// Tensor-core router of bf16 layers (same outputs as launch_router).
+cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids,
+                             const float* bias, int* topk_idx, float* topk_gate, int* tile_counts,
+                             float* tile_psum, int* status, cudaStream_t st);
+
+// Row-major bf16 [rows, cols] as a 2D TMA map, box [box_rows x 64], 128-byte swizzle.
+bool encode_bf16_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                     int box_rows);
 
 // Per-tile histogram of topk_idx (used when the router's tile histogram is not at hand).
 cudaError_t launch_tile_hist(const Dims& m, const int* topk_idx, int* tile_counts, int* status,
                              cudaStream_t st);
 
-// Offsets [N+1] and per-tile bases from the tile histograms; checks them against `counts`
-// (may be null).
-cudaError_t launch_perm_scan(const Dims& m, const int* tile_counts, const int* counts,
-                             int* offsets, int* tile_base, int* status, cudaStream_t st);
+// Reduction of the per-tile router results in tile order (one CTA). Every output is optional.
+struct FinalizeArgs {
+    Dims m;
+    int n_tiles;
+    const int* tile_counts;   // [n_tiles, N]
+    const float* tile_psum;   // [n_tiles, N] or null
+    int* counts_out;          // [N]: tokens per expert
+    float* psum_out;          // [N]: sum of affinities
+    const int* counts_check;  // [N]: caller counts to verify (MOE_ERR_CORRUPT_INPUT on mismatch)
+    int* offsets;             // [N+1]: exclusive scan of the totals
+    int* tile_base;           // [n_tiles, N]: first row of a tile's tokens inside expert j
+    float* f_out;             // [N] balance statistics
+    float* P_out;             // [N]
+    float* losses;            // [2]
+    int* status;
+};
+cudaError_t launch_route_finalize(const FinalizeArgs& a, cudaStream_t st);
 
-// perm_token / perm_slot from topk_idx and the per-tile bases.
-cudaError_t launch_perm_scatter(const Dims& m, const int* topk_idx, const int* tile_base,
-                                int* perm_token, int* perm_slot, cudaStream_t st);
+// perm_token / perm_slot from topk_idx, the offsets and the per-tile bases.
+cudaError_t launch_perm_scatter(const Dims& m, const int* topk_idx, const int* offsets,
+                                const int* tile_base, int* perm_token, int* perm_slot,
+                                cudaStream_t st);
 
 // x_perm[perm_slot[t*K+k]] = u[t].
 cudaError_t launch_gather(const Dims& m, const void* u, const int* perm_slot, void* x_perm,

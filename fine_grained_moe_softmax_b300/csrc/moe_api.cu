@@ -151,9 +151,17 @@ int moe_route(const moe_config* cfg, const void* u, const void* centroids,
     cudaError_t e = launch_router(m, u, centroids, logit_bias, topk_idx, topk_gate,
                                   at<int>(ws, L.tile_counts), at<float>(ws, L.tile_psum), status,
                                   st);
-    if (e == cudaSuccess)
-        e = launch_route_reduce(m, at<int>(ws, L.tile_counts), at<float>(ws, L.tile_psum),
-                                counts, psum, st);
+    if (e == cudaSuccess) {
+        FinalizeArgs fa{};
+        fa.m = m;
+        fa.n_tiles = L.n_tiles;
+        fa.tile_counts = at<int>(ws, L.tile_counts);
+        fa.tile_psum = at<float>(ws, L.tile_psum);
+        fa.counts_out = counts;
+        fa.psum_out = psum;
+        fa.status = status;
+        e = launch_route_finalize(fa, st);
+    }
     return cuda_rc(e);
 }
 
@@ -173,8 +181,19 @@ int moe_permute(const moe_config* cfg, const int32_t* topk_idx, const int32_t* c
     int* tc = at<int>(ws, L.tile_counts);
     int* tb = at<int>(ws, L.tile_base);
     cudaError_t e = launch_tile_hist(m, topk_idx, tc, status, st);
-    if (e == cudaSuccess) e = launch_perm_scan(m, tc, counts, offsets, tb, status, st);
-    if (e == cudaSuccess) e = launch_perm_scatter(m, topk_idx, tb, perm_token, perm_slot, st);
+    if (e == cudaSuccess) {
+        FinalizeArgs fa{};
+        fa.m = m;
+        fa.n_tiles = L.n_tiles;
+        fa.tile_counts = tc;
+        fa.counts_check = counts;
+        fa.offsets = offsets;
+        fa.tile_base = tb;
+        fa.status = status;
+        e = launch_route_finalize(fa, st);
+    }
+    if (e == cudaSuccess)
+        e = launch_perm_scatter(m, topk_idx, offsets, tb, perm_token, perm_slot, st);
     return cuda_rc(e);
 }
 
@@ -257,10 +276,25 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
     mk.mark(0);
     cudaError_t e = launch_router(m, u, centroids, logit_bias, topk_idx, topk_gate, tc, tp, status,
                                   st);
-    if (e == cudaSuccess) e = launch_route_reduce(m, tc, tp, counts, psum, st);
     mk.mark(1);
-    if (e == cudaSuccess) e = launch_perm_scan(m, tc, nullptr, offsets, tb, status, st);
-    if (e == cudaSuccess) e = launch_perm_scatter(m, topk_idx, tb, perm_token, perm_slot, st);
+    if (e == cudaSuccess) {   // totals, offsets, tile bases and the balance statistics
+        FinalizeArgs fa{};
+        fa.m = m;
+        fa.n_tiles = L.n_tiles;
+        fa.tile_counts = tc;
+        fa.tile_psum = tp;
+        fa.counts_out = counts;
+        fa.psum_out = psum;
+        fa.offsets = offsets;
+        fa.tile_base = tb;
+        fa.f_out = f;
+        fa.P_out = P;
+        fa.losses = losses;
+        fa.status = status;
+        e = launch_route_finalize(fa, st);
+    }
+    if (e == cudaSuccess)
+        e = launch_perm_scatter(m, topk_idx, offsets, tb, perm_token, perm_slot, st);
     mk.mark(2);
     if (e == cudaSuccess) e = launch_gather(m, u, perm_slot, at<void>(ws, L.x_perm), status, st);
     mk.mark(3);
@@ -272,8 +306,7 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
     if (e == cudaSuccess)
         e = launch_combine(m, u, at<void>(ws, L.y_r), at<void>(ws, L.y_s), perm_slot, topk_gate, h,
                            status, st);
-    mk.mark(6);
-    if (e == cudaSuccess) e = launch_balance(m, counts, psum, f, P, losses, st);
+    mk.mark(6);   // the statistics were produced by the finalize kernel of the permute stage
     mk.mark(7);
     return cuda_rc(e);
 }

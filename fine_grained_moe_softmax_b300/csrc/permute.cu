@@ -33,25 +33,47 @@ __global__ void tile_hist_kernel(Dims m, const int* __restrict__ topk_idx,
         tile_counts[(size_t)tile * m.N + j] = hist[j];
 }
 
-// One CTA: per expert, the running base over tiles (token order), the total, the check against
-// the caller's counts, then offsets by an exclusive scan over experts.
-__global__ void perm_scan_kernel(Dims m, int n_tiles, const int* __restrict__ tile_counts,
-                                 const int* __restrict__ counts, int* __restrict__ offsets,
-                                 int* __restrict__ tile_base, int* status) {
+// One CTA of 32 warps. Warp w handles experts w, w+32, ...: its lanes walk the tiles 32 at a time
+// (tile = chunk + lane), a warp scan gives each tile's base inside the expert (token order), and a
+// fixed-pattern butterfly sums the tile affinity sums, so the result is the same on every run.
+// Optional outputs: counts / psum (router totals), offsets (exclusive scan over experts), the
+// balance statistics, and a check of the totals against caller-supplied counts.
+__global__ void __launch_bounds__(1024) route_finalize_kernel(FinalizeArgs a) {
     __shared__ int total[kMaxRouted];
+    __shared__ float ptot[kMaxRouted];
     __shared__ int off[kMaxRouted + 1];
-    const int N = m.N;
-    for (int j = threadIdx.x; j < N; j += blockDim.x) {
-        int run = 0;
-        for (int tile = 0; tile < n_tiles; ++tile) {
-            tile_base[(size_t)tile * N + j] = run;
-            run += tile_counts[(size_t)tile * N + j];
+    const Dims m = a.m;
+    const int N = m.N, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = warp; j < N; j += 32) {
+        int carry = 0;
+        float p = 0.f;
+        for (int c0 = 0; c0 < a.n_tiles; c0 += 32) {
+            const int tile = c0 + lane;
+            const bool in = tile < a.n_tiles;
+            const int c = in ? a.tile_counts[(size_t)tile * N + j] : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (a.tile_base && in) a.tile_base[(size_t)tile * N + j] = carry + incl - c;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+            if (a.tile_psum && in) p += a.tile_psum[(size_t)tile * N + j];
         }
-        total[j] = run;
-        if (counts && counts[j] != run) set_status(status, MOE_ERR_CORRUPT_INPUT);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+        if (lane == 0) {
+            total[j] = carry;
+            ptot[j] = p;
+            if (a.counts_out) a.counts_out[j] = carry;
+            if (a.psum_out) a.psum_out[j] = p;
+            if (a.counts_check && a.counts_check[j] != carry)
+                set_status(a.status, MOE_ERR_CORRUPT_INPUT);
+        }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && a.offsets) {
         int acc = 0;
         for (int j = 0; j < N; ++j) {
             off[j] = acc;
@@ -59,35 +81,85 @@ __global__ void perm_scan_kernel(Dims m, int n_tiles, const int* __restrict__ ti
         }
         off[N] = acc;
     }
-    __syncthreads();
-    for (int j = threadIdx.x; j <= N; j += blockDim.x) offsets[j] = off[j];
-    for (int j = threadIdx.x; j < N; j += blockDim.x)
-        for (int tile = 0; tile < n_tiles; ++tile) tile_base[(size_t)tile * N + j] += off[j];
-}
-
-// One CTA per tile: thread j walks the tile's assignments in (token, slot) order and hands out
-// consecutive rows of expert j, which keeps tokens ascending inside every expert.
-__global__ void perm_scatter_kernel(Dims m, const int* __restrict__ topk_idx,
-                                    const int* __restrict__ tile_base, int* __restrict__ perm_token,
-                                    int* __restrict__ perm_slot) {
-    __shared__ int idx_s[kRouteTile * kMaxTopK];
-    const int tile = blockIdx.x, t0 = tile * kRouteTile, K = m.K;
-    const int n = min(kRouteTile, m.T - t0) * K;
-    for (int a = threadIdx.x; a < n; a += blockDim.x) {
-        const int j = topk_idx[(size_t)t0 * K + a];
-        idx_s[a] = j;
-        if (j < 0 || j >= m.N) perm_slot[(size_t)t0 * K + a] = -1;   // flagged by the histogram
+    if (threadIdx.x == 32 && a.losses) {   // balance statistics, same arithmetic as balance_kernel
+        const float Tf = (float)max(m.T, 1);
+        const float scale = (float)N / ((float)m.K * Tf);
+        float lexp = 0.f, ldev = 0.f;
+        for (int j = 0; j < N; ++j) lexp += (scale * (float)total[j]) * (ptot[j] / Tf);
+        const int base = N / m.D, extra = N % m.D;
+        int first = 0;
+        for (int g = 0; g < m.D; ++g) {
+            const int size = base + (g < extra ? 1 : 0);
+            float fs = 0.f, ps = 0.f;
+            for (int j = first; j < first + size; ++j) {
+                fs += scale * (float)total[j];
+                ps += ptot[j] / Tf;
+            }
+            ldev += (fs / (float)size) * ps;
+            first += size;
+        }
+        a.losses[0] = m.a1 * lexp;
+        a.losses[1] = m.a2 * ldev;
     }
     __syncthreads();
-    for (int j = threadIdx.x; j < m.N; j += blockDim.x) {
-        int row = tile_base[(size_t)tile * m.N + j];
-        for (int a = 0; a < n; ++a) {
-            if (idx_s[a] == j) {
-                perm_token[row] = t0 + a / K;
-                perm_slot[(size_t)t0 * K + a] = row;
-                ++row;
-            }
+    if (a.offsets)
+        for (int j = threadIdx.x; j <= N; j += blockDim.x) a.offsets[j] = off[j];
+    if (a.f_out) {
+        const float Tf = (float)max(m.T, 1);
+        const float scale = (float)N / ((float)m.K * Tf);
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            a.f_out[j] = scale * (float)total[j];
+            a.P_out[j] = ptot[j] / Tf;
         }
+    }
+}
+
+// One CTA per 128-token tile. Each assignment a = t_local*K' + k sets bit a of its expert's
+// bitmap; the row of an assignment is offsets[j] + the tile's base for j + the number of
+// earlier assignments of the tile to j (a prefix popcount). Assignment order is token-major, so
+// tokens stay ascending inside every expert, and the result does not depend on thread timing.
+__global__ void __launch_bounds__(256) perm_scatter_kernel(Dims m, const int* __restrict__ topk_idx,
+                                                         const int* __restrict__ offsets,
+                                                         const int* __restrict__ tile_base,
+                                                         int* __restrict__ perm_token,
+                                                         int* __restrict__ perm_slot) {
+    extern __shared__ uint32_t sm[];
+    const int K = m.K, N = m.N, W = (kRouteTile * K + 31) / 32;   // words per expert bitmap
+    uint32_t* bits = sm;                                        // [N][W]
+    int* pre = reinterpret_cast<int*>(bits + (size_t)N * W);     // [N][W] popcount prefix
+    int* base = pre + (size_t)N * W;                            // [N]
+    const int tile = blockIdx.x, t0 = tile * kRouteTile;
+    const int n = min(kRouteTile, m.T - t0) * K;
+    for (int i = threadIdx.x; i < N * W; i += blockDim.x) bits[i] = 0u;
+    for (int j = threadIdx.x; j < N; j += blockDim.x)
+        base[j] = offsets[j] + tile_base[(size_t)tile * N + j];
+    __syncthreads();
+    const int* idx = topk_idx + (size_t)t0 * K;
+    for (int a = threadIdx.x; a < n; a += blockDim.x) {
+        const int j = idx[a];
+        if (j >= 0 && j < N) atomicOr(&bits[(size_t)j * W + (a >> 5)], 1u << (a & 31));
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+        int acc = 0;
+        for (int w = 0; w < W; ++w) {
+            pre[(size_t)j * W + w] = acc;
+            acc += __popc(bits[(size_t)j * W + w]);
+        }
+    }
+    __syncthreads();
+    for (int a = threadIdx.x; a < n; a += blockDim.x) {
+        const int j = idx[a];
+        if (j < 0 || j >= N) {
+            perm_slot[(size_t)t0 * K + a] = -1;   // flagged by the histogram
+            continue;
+        }
+        const int w = a >> 5;
+        const int rank = pre[(size_t)j * W + w] +
+                         __popc(bits[(size_t)j * W + w] & ((1u << (a & 31)) - 1u));
+        const int row = base[j] + rank;
+        perm_token[row] = t0 + a / K;
+        perm_slot[(size_t)t0 * K + a] = row;
     }
 }
 
@@ -159,22 +231,24 @@ cudaError_t launch_tile_hist(const Dims& m, const int* topk_idx, int* tile_count
     return cudaGetLastError();
 }
 
-cudaError_t launch_perm_scan(const Dims& m, const int* tile_counts, const int* counts,
-                             int* offsets, int* tile_base, int* status, cudaStream_t st) {
-    const int n_tiles = (m.T + kRouteTile - 1) / kRouteTile;
-    perm_scan_kernel<<<1, 256, 0, st>>>(m, n_tiles, tile_counts, counts, offsets, tile_base,
-                                        status);
+cudaError_t launch_route_finalize(const FinalizeArgs& a, cudaStream_t st) {
+    route_finalize_kernel<<<1, 1024, 0, st>>>(a);
     note_launches(1);
     return cudaGetLastError();
 }
 
-cudaError_t launch_perm_scatter(const Dims& m, const int* topk_idx, const int* tile_base,
-                                int* perm_token, int* perm_slot, cudaStream_t st) {
+cudaError_t launch_perm_scatter(const Dims& m, const int* topk_idx, const int* offsets,
+                                const int* tile_base, int* perm_token, int* perm_slot,
+                                cudaStream_t st) {
     const int n_tiles = (m.T + kRouteTile - 1) / kRouteTile;
     if (n_tiles == 0) return cudaSuccess;
-    const int threads = ((m.N + 31) / 32) * 32;
-    perm_scatter_kernel<<<n_tiles, threads, 0, st>>>(m, topk_idx, tile_base, perm_token,
-                                                     perm_slot);
+    const int W = (kRouteTile * m.K + 31) / 32;
+    const size_t smem = (size_t)m.N * W * 8 + (size_t)m.N * 4;
+    cudaError_t e = cudaFuncSetAttribute(perm_scatter_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    perm_scatter_kernel<<<n_tiles, 256, smem, st>>>(m, topk_idx, offsets, tile_base, perm_token,
+                                                    perm_slot);
     note_launches(1);
     return cudaGetLastError();
 }

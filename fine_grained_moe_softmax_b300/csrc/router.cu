@@ -1,4 +1,4 @@
-// router.cu -- token-to-centroid affinities, softmax, top-k and gates.
+// router.cu -- router of fp32 layers on the CUDA cores (bf16 layers: router_tc.cu).
 //
 // [P1] "DeepSeekMoE 论文解读" (xxmr.cn), §方法细节: gates g_{i,t} come from Topk({s_{j,t}}, mK);
 //      the K_s shared experts are always active, so routing ranks only the N' routed experts.
@@ -57,10 +57,6 @@ template <typename E> struct Pair;
 template <> struct Pair<float> {
     using V = float2;
     __device__ static float2 f2(V x) { return x; }
-};
-template <> struct Pair<__nv_bfloat16> {
-    using V = __nv_bfloat162;
-    __device__ static float2 f2(V x) { return __bfloat1622float2(x); }
 };
 
 // One CTA per 128-token tile. Phase 1: each warp computes the logits of its tokens (lanes split
@@ -152,21 +148,6 @@ router_simt_kernel(const E* __restrict__ u, const E* __restrict__ cent,
     }
 }
 
-__global__ void route_reduce_kernel(Dims m, int n_tiles, const int* __restrict__ tile_counts,
-                                    const float* __restrict__ tile_psum, int* __restrict__ counts,
-                                    float* __restrict__ psum) {
-    for (int j = threadIdx.x; j < m.N; j += blockDim.x) {
-        int c = 0;
-        float p = 0.f;
-        for (int tile = 0; tile < n_tiles; ++tile) {
-            c += tile_counts[(size_t)tile * m.N + j];
-            p += tile_psum[(size_t)tile * m.N + j];
-        }
-        counts[j] = c;
-        psum[j] = p;
-    }
-}
-
 template <typename E, int KMAX>
 cudaError_t launch_router_t(const Dims& m, const void* u, const void* cent, const float* bias,
                             int* idx, float* gate, int* tc, float* tp, int* status,
@@ -190,25 +171,13 @@ cudaError_t launch_router(const Dims& m, const void* u, const void* centroids, c
                           int* topk_idx, float* topk_gate, int* tile_counts, float* tile_psum,
                           int* status, cudaStream_t st) {
     if (m.T == 0) return cudaSuccess;
-    const bool small_k = m.K <= 8;
-    if (m.dtype == MOE_DTYPE_F32)
-        return small_k ? launch_router_t<float, 8>(m, u, centroids, bias, topk_idx, topk_gate,
-                                                   tile_counts, tile_psum, status, st)
-                       : launch_router_t<float, 16>(m, u, centroids, bias, topk_idx, topk_gate,
-                                                    tile_counts, tile_psum, status, st);
-    return small_k ? launch_router_t<__nv_bfloat16, 8>(m, u, centroids, bias, topk_idx, topk_gate,
-                                                       tile_counts, tile_psum, status, st)
-                   : launch_router_t<__nv_bfloat16, 16>(m, u, centroids, bias, topk_idx,
-                                                        topk_gate, tile_counts, tile_psum,
-                                                        status, st);
-}
-
-cudaError_t launch_route_reduce(const Dims& m, const int* tile_counts, const float* tile_psum,
-                                int* counts, float* psum, cudaStream_t st) {
-    const int n_tiles = (m.T + kRouteTile - 1) / kRouteTile;
-    route_reduce_kernel<<<1, 256, 0, st>>>(m, n_tiles, tile_counts, tile_psum, counts, psum);
-    note_launches(1);
-    return cudaGetLastError();
+    if (m.dtype == MOE_DTYPE_BF16)
+        return launch_router_tc(m, u, centroids, bias, topk_idx, topk_gate, tile_counts,
+                                tile_psum, status, st);
+    return m.K <= 8 ? launch_router_t<float, 8>(m, u, centroids, bias, topk_idx, topk_gate,
+                                                tile_counts, tile_psum, status, st)
+                    : launch_router_t<float, 16>(m, u, centroids, bias, topk_idx, topk_gate,
+                                                 tile_counts, tile_psum, status, st);
 }
 
 }  // namespace moe

@@ -1,0 +1,357 @@
+// router_tc.cu -- router of bf16 layers on the tensor cores.
+//
+// [P1] "DeepSeekMoE 论文解读" (xxmr.cn), §方法细节: gates come from Topk({s_{j,t}}, mK) over the
+//      routed experts (the K_s shared experts are always active and are not ranked).
+// [P2] "【论文总结】MoE" (mickeyding.github.io), §2.2: s_{j,t} = softmax_j(u_t . e_j) against the
+//      learnable centroids e_j; §2.3: f_i counts selections, P_i averages s over the T tokens.
+//
+// The logits of a 128-token tile are one [128 x d] x [d x N'] product: the tile's token rows and
+// the centroids stream through a TMA ring into tcgen05.mma (M = 128, N = N' rounded up to 32),
+// accumulating fp32 logits in TMEM. Four epilogue warps then own one token per thread: each reads
+// its logit row from TMEM (warp w sees TMEM lanes 32*(w%4) .. +31), adds the optional bias, and
+// computes the softmax, a register top-K' (ranked by logit; the lower index wins ties), the gates,
+// the tile's expert histogram and, by a warp transpose-reduction, the tile's per-expert sums of
+// affinities in a fixed order.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+#include "waits.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int RBM = 128;
+constexpr int RBK = 64;
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 8;
+
+struct RouterArgs {
+    CUtensorMap a;        // u [T, d], box [128 x 64]
+    CUtensorMap b;        // centroids [N', d], box [n_pad x 64]
+    const float* bias;    // [N'] or null
+    int T, N, K, renorm, k_blocks, n_pad, stages, tmem_cols;
+    uint32_t stage_bytes;
+    int* topk_idx;
+    float* topk_gate;
+    int* tile_counts;
+    float* tile_psum;
+    int* status;
+};
+
+template <int KMAX>
+struct TopK {
+    float v[KMAX];
+    int i[KMAX];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) {
+            v[q] = -INFINITY;
+            i[q] = -1;
+        }
+    }
+    // candidates arrive in ascending expert index; only a strictly larger value displaces
+    __device__ __forceinline__ void push(float x, int j) {
+        if (!(x > v[KMAX - 1])) return;
+#pragma unroll
+        for (int q = KMAX - 1; q > 0; --q) {
+            if (x > v[q]) {
+                if (x > v[q - 1]) {
+                    v[q] = v[q - 1];
+                    i[q] = i[q - 1];
+                } else {
+                    v[q] = x;
+                    i[q] = j;
+                }
+            }
+        }
+        if (x > v[0]) {
+            v[0] = x;
+            i[0] = j;
+        }
+    }
+};
+
+// One halving step of the warp transpose-reduction: lanes with bit HALF clear keep columns
+// [0, HALF) of their block and receive the partner's; lanes with it set keep [HALF, 2*HALF).
+template <int HALF>
+__device__ __forceinline__ void halve(float (&v)[32], bool upper) {
+#pragma unroll
+    for (int i = 0; i < HALF; ++i) {
+        const float send = upper ? v[i] : v[i + HALF];
+        const float keep = upper ? v[i + HALF] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, HALF);
+    }
+}
+
+// After this, lane l of the warp holds the sum over the 32 lanes of column l of v[0..31].
+__device__ __forceinline__ float column_sums(float (&v)[32], int lane) {
+    halve<16>(v, lane & 16);
+    halve<8>(v, lane & 8);
+    halve<4>(v, lane & 4);
+    halve<2>(v, lane & 2);
+    halve<1>(v, lane & 1);
+    return v[0];
+}
+
+__device__ __forceinline__ void epilogue_bar() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_constant__ RouterArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t ring = a.stages * a.stage_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + ring);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* tfull = empty + kMaxStages;
+    uint64_t* drain = tfull + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    float* colsum = reinterpret_cast<float*>(tmem_holder + 4);   // [4][kMaxRouted]
+    int* hist = reinterpret_cast<int*>(colsum + 4 * kMaxRouted);  // [kMaxRouted]
+    float* bias_s = reinterpret_cast<float*>(hist + kMaxRouted);  // [kMaxRouted]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x;
+    const int N = a.N, K = a.K;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(tfull), 1);
+        ptx::mbar_init(ptx::smem_addr(drain), 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    for (int j = threadIdx.x; j < kMaxRouted; j += blockDim.x) {
+        hist[j] = 0;
+        bias_s[j] = (a.bias && j < N) ? a.bias[j] : 0.f;
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&a.a);
+        ptx::prefetch_tmap(&a.b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), a.tmem_cols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int kb = 0; kb < a.k_blocks; ++kb) {
+                if (!wait_phase(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = ptx::smem_addr(&full[stage]);
+                uint8_t* st = base + stage * a.stage_bytes;
+                ptx::mbar_arrive_expect_tx(fb, a.stage_bytes);
+                ptx::tma_load_2d(ptx::smem_addr(st), &a.a, kb * RBK, tile * RBM, fb);
+                ptx::tma_load_2d(ptx::smem_addr(st + RBM * RBK * 2), &a.b, kb * RBK, 0, fb);
+                ++issued;
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) {
+                for (int i = 0; i < issued && i < a.stages; ++i) {
+                    if (--stage < 0) {
+                        stage = a.stages - 1;
+                        phase ^= 1;
+                    }
+                    drain_wait(ptx::smem_addr(&full[stage]), phase);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------- MMA issuer ----
+        if (lane == 0) {
+            const uint32_t idesc = ptx::idesc_bf16_f32(RBM, a.n_pad);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true, any = false;
+            for (int kb = 0; kb < a.k_blocks; ++kb) {
+                if (!wait_phase(ptx::smem_addr(&full[stage]), phase, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t a0 = ptx::smem_addr(base + stage * a.stage_bytes);
+                const uint32_t b0 = a0 + RBM * RBK * 2;
+#pragma unroll
+                for (int k = 0; k < RBK / 16; ++k)
+                    ptx::mma_f16(tmem, ptx::sw128_kmajor_desc(a0 + k * 32),
+                                 ptx::sw128_kmajor_desc(b0 + k * 32), idesc,
+                                 (kb | k) != 0 ? 1u : 0u);
+                any = true;
+                ptx::mma_commit(ptx::smem_addr(&empty[stage]));
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (ok) ptx::mma_commit(ptx::smem_addr(tfull));
+            else if (any) {
+                ptx::mma_commit(ptx::smem_addr(drain));
+                drain_wait(ptx::smem_addr(drain), 0);
+            }
+        }
+    } else {
+        // --------------------------------------------------------------------- epilogue ----
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int t = tile * RBM + row;
+        const bool valid = t < a.T;
+        int ok = 1;
+        if (lane == 0) ok = wait_phase(ptx::smem_addr(tfull), 0, abort_flag, a.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        const int n_chunks = a.n_pad / 32;
+        if (ok) {
+            ptx::tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16);
+            // pass 1: largest logit and the top-K' list
+            float zmax = -INFINITY;
+            TopK<KMAX> top;
+            top.init();
+            for (int c = 0; c < n_chunks; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(tb + c * 32, v);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = c * 32 + i;
+                    if (j < N) {
+                        const float z = __uint_as_float(v[i]) + bias_s[j];
+                        zmax = fmaxf(zmax, z);
+                        top.push(z, j);
+                    }
+                }
+            }
+            // pass 2: softmax denominator
+            float sum = 0.f;
+            for (int c = 0; c < n_chunks; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(tb + c * 32, v);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = c * 32 + i;
+                    if (j < N) sum += expf(__uint_as_float(v[i]) + bias_s[j] - zmax);
+                }
+            }
+            const float inv = 1.0f / sum;
+            if (valid) {
+                float gsum = 0.f;
+#pragma unroll
+                for (int q = 0; q < KMAX; ++q)
+                    if (q < K) gsum += expf(top.v[q] - zmax) * inv;
+                bool bad = !(zmax < INFINITY);
+#pragma unroll
+                for (int q = 0; q < KMAX; ++q) {
+                    if (q < K) {
+                        int j = top.i[q];
+                        if (j < 0) {
+                            bad = true;
+                            j = 0;
+                        }
+                        const float s = expf(top.v[q] - zmax) * inv;
+                        a.topk_idx[(size_t)t * K + q] = j;
+                        a.topk_gate[(size_t)t * K + q] = a.renorm ? s / gsum : s;
+                        atomicAdd(&hist[j], 1);
+                    }
+                }
+                if (bad) set_status(a.status, MOE_ERR_CORRUPT_INPUT);
+            }
+            // pass 3: affinities, summed over this warp's 32 tokens per expert column
+            for (int c = 0; c < n_chunks; ++c) {
+                uint32_t v[32];
+                ptx::tmem_ld_32x32b_x32(tb + c * 32, v);
+                ptx::tmem_ld_wait();
+                float s[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = c * 32 + i;
+                    s[i] = (valid && j < N) ? expf(__uint_as_float(v[i]) + bias_s[j] - zmax) * inv
+                                            : 0.f;
+                }
+                const float col = column_sums(s, lane);
+                colsum[quarter * kMaxRouted + c * 32 + lane] = col;
+            }
+        }
+        ptx::tc_fence_before();
+        epilogue_bar();
+        if (ok) {
+            const int et = threadIdx.x - 64;   // 0..127 over the four epilogue warps
+            for (int j = et; j < N; j += 128) {
+                a.tile_psum[(size_t)tile * N + j] =
+                    ((colsum[j] + colsum[kMaxRouted + j]) + colsum[2 * kMaxRouted + j]) +
+                    colsum[3 * kMaxRouted + j];
+                a.tile_counts[(size_t)tile * N + j] = hist[j];
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, a.tmem_cols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids,
+                             const float* bias, int* topk_idx, float* topk_gate, int* tile_counts,
+                             float* tile_psum, int* status, cudaStream_t st) {
+    RouterArgs a{};
+    a.n_pad = (m.N + 31) / 32 * 32;
+    if (!encode_bf16_map(&a.a, u, (uint64_t)m.T, (uint64_t)m.d, RBM) ||
+        !encode_bf16_map(&a.b, centroids, (uint64_t)m.N, (uint64_t)m.d, a.n_pad))
+        return cudaErrorInvalidValue;
+    a.bias = bias;
+    a.T = m.T;
+    a.N = m.N;
+    a.K = m.K;
+    a.renorm = m.renorm;
+    a.k_blocks = m.d / RBK;
+    a.stage_bytes = (uint32_t)(RBM * RBK * 2 + a.n_pad * RBK * 2);
+    a.stages = (int)std::min<uint32_t>(kMaxStages, (192u * 1024u) / a.stage_bytes);
+    int cols = 32;
+    while (cols < a.n_pad) cols *= 2;
+    a.tmem_cols = cols;
+    a.topk_idx = topk_idx;
+    a.topk_gate = topk_gate;
+    a.tile_counts = tile_counts;
+    a.tile_psum = tile_psum;
+    a.status = status;
+    const size_t smem = 1024 + (size_t)a.stages * a.stage_bytes + 8 * (2 * kMaxStages + 2) + 16 +
+                        4 * (4 * kMaxRouted + 2 * kMaxRouted);
+    const int n_tiles = (m.T + RBM - 1) / RBM;
+    auto kern = m.K <= 8 ? router_tc_kernel<8> : router_tc_kernel<16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<n_tiles, kThreads, smem, st>>>(a);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
