@@ -44,6 +44,21 @@ def gate_up_flops(sh, T) -> float:
     return 4.0 * sh.d * sh.inter * T * (sh.n_shared + sh.top_k)
 
 
+def gate_up_traffic(workload: str):
+    """DRAM bytes (read + write) of one gate/up GEMM launch from the committed ncu summary, or
+    None when the workload was not captured."""
+    path = os.path.join(ROOT, "profiles", "gemm_traffic_full_size.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 5 and not line.startswith("#") and parts[0] == workload \
+                    and parts[1] == "gemm_gate_up":
+                return int(parts[2]) + int(parts[3])
+    return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -208,6 +223,17 @@ def run_ours(args, sh, rank, world, local_rank):
     status = layer.device_status()
     if status != 0:
         raise RuntimeError(f"device status {moe.moe_status_string(status)} after warm-up")
+    graph, graph_kernels = (layer.capture(u) if args.graph else (None, 0))
+    if graph is not None:
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
+    def step():
+        if graph is not None:
+            graph.replay()
+        else:
+            layer.forward(u)
 
     # ---- device-resident timing: every step timed on its own, L2 flushed in between ----
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -215,20 +241,30 @@ def run_ours(args, sh, rank, world, local_rank):
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    moe.moe_profile_enable(True, args.steps)
+    if graph is None:
+        moe.moe_profile_enable(True, args.steps)
     barrier()
     torch.cuda.synchronize(dev)
     launches0 = moe.moe_launch_count()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         starts[i].record(stream)
-        layer.forward(u)
+        step()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    launches = moe.moe_launch_count() - launches0
-    stage_ms, n_prof = moe.moe_profile_read()
-    moe.moe_profile_enable(False)
+    launches = moe.moe_launch_count() - launches0 + graph_kernels * args.steps
+    if graph is None:
+        stage_ms, n_prof = moe.moe_profile_read()
+        moe.moe_profile_enable(False)
+    else:   # stage times come from a separate profiled pass of direct calls
+        moe.moe_profile_enable(True, args.steps)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            layer.forward(u)
+        torch.cuda.synchronize(dev)
+        stage_ms, n_prof = moe.moe_profile_read()
+        moe.moe_profile_enable(False)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
 
@@ -273,11 +309,7 @@ def run_ours(args, sh, rank, world, local_rank):
     gu_ms = stage_ms["gemm_gate_up"] / max(n_prof, 1)
     gu_tflops = gate_up_flops(sh, T) / (gu_ms / 1e3) / 1e12
     layer_tflops = flops_per_token(sh) * T / (total_ms / args.steps / 1e3) / 1e12
-    traffic = None
-    prof_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof_path):
-        with open(prof_path) as f:
-            traffic = json.load(f).get(sh.name, {}).get("gemm_gate_up_bytes")
+    traffic = gate_up_traffic(sh.name)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -287,6 +319,8 @@ def run_ours(args, sh, rank, world, local_rank):
                    "n_routed": sh.n_routed, "inter": sh.inter, "top_k": sh.top_k,
                    "global_batch": T * world, "parallelism": f"replicas x{world}",
                    "l2": "flushed between timed steps (512 MB write outside the events)",
+                   "launch": "CUDA graph replay of moe_layer_forward" if graph is not None
+                             else "direct moe_layer_forward calls",
                    "inputs": "seeded Gaussian tensors of the workload's shape"},
         "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel (gate/up + SwiGLU epilogue)",
                      "achieved": gu_tflops, "peak": bf16_tf, "unit": "TFLOP/s",
@@ -319,6 +353,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=512)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time CUDA-graph replays of the layer call instead of direct calls")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (small profiling captures only; not a bench line)")
     args = ap.parse_args()

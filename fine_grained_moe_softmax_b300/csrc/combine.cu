@@ -45,42 +45,61 @@ template <> struct Vec<__nv_bfloat16> {
     }
 };
 
-// One warp per token; each lane owns 16-byte column vectors. fp32 accumulation in the fixed
-// order u, shared sum, routed k = 0..K'-1.
-template <typename E>
-__global__ void combine_kernel(Dims m, const E* __restrict__ u, const E* __restrict__ y_r,
-                               const E* __restrict__ y_s, const int* __restrict__ perm_slot,
-                               const float* __restrict__ gate, E* __restrict__ h, int* status) {
+// One CTA per token; thread i owns 16-byte column vectors i, i + blockDim, ... of the row (one
+// vector each for d <= 8 * blockDim in bf16). All 2 + KMAX row vectors of an iteration are loaded
+// before any is used (slots k >= K' and bad rows read row 0 and are masked out), so every thread
+// keeps that many loads in flight. fp32 accumulation in the fixed order u, shared sum, routed
+// k = 0..K'-1.
+template <typename E, int KMAX>
+__global__ void __launch_bounds__(256) combine_kernel(Dims m, const E* __restrict__ u,
+                                                      const E* __restrict__ y_r,
+                                                      const E* __restrict__ y_s,
+                                                      const int* __restrict__ perm_slot,
+                                                      const float* __restrict__ gate,
+                                                      E* __restrict__ h, int* status) {
     constexpr int VN = Vec<E>::n;
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (t >= m.T) return;
+    const int t = blockIdx.x;
     const long TK = (long)m.T * m.K;
-    int rows[kMaxTopK];
-    float g[kMaxTopK];
+    int rows[KMAX];
+    float g[KMAX];
+    bool use[KMAX];
     bool bad = false;
 #pragma unroll
-    for (int k = 0; k < kMaxTopK; ++k) {
-        rows[k] = -1;
+    for (int k = 0; k < KMAX; ++k) {
+        rows[k] = 0;
         g[k] = 0.f;
+        use[k] = false;
         if (k < m.K) {
-            rows[k] = perm_slot[(size_t)t * m.K + k];
-            g[k] = gate[(size_t)t * m.K + k];
-            if (rows[k] < 0 || rows[k] >= TK) { bad = true; rows[k] = -1; }
+            const int r = perm_slot[(size_t)t * m.K + k];
+            if (r < 0 || r >= TK) {
+                bad = true;
+            } else {
+                rows[k] = r;
+                g[k] = gate[(size_t)t * m.K + k];
+                use[k] = true;
+            }
         }
     }
-    if (bad && lane == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
-    for (int c = lane * VN; c < m.d; c += 32 * VN) {
+    if (bad && threadIdx.x == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
+    const bool shared = m.Ks > 0;
+    for (int c = threadIdx.x * VN; c < m.d; c += blockDim.x * VN) {
+        uint4 raw_u = *reinterpret_cast<const uint4*>(u + (size_t)t * m.d + c);
+        uint4 raw_s = shared ? *reinterpret_cast<const uint4*>(y_s + (size_t)t * m.d + c) : raw_u;
+        uint4 raw_r[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            raw_r[k] = *reinterpret_cast<const uint4*>(y_r + (size_t)rows[k] * m.d + c);
         float acc[VN], y[VN];
-        Vec<E>::load(u + (size_t)t * m.d + c, acc);
-        if (m.Ks > 0) {
-            Vec<E>::load(y_s + (size_t)t * m.d + c, y);
+        Vec<E>::load(&raw_u, acc);
+        if (shared) {
+            Vec<E>::load(&raw_s, y);
 #pragma unroll
             for (int q = 0; q < VN; ++q) acc[q] += y[q];
         }
 #pragma unroll
-        for (int k = 0; k < kMaxTopK; ++k) {
-            if (k < m.K && rows[k] >= 0) {
-                Vec<E>::load(y_r + (size_t)rows[k] * m.d + c, y);
+        for (int k = 0; k < KMAX; ++k) {
+            if (use[k]) {
+                Vec<E>::load(&raw_r[k], y);
 #pragma unroll
                 for (int q = 0; q < VN; ++q) acc[q] = fmaf(g[k], y[q], acc[q]);
             }
@@ -129,20 +148,30 @@ __global__ void balance_kernel(Dims m, const int* __restrict__ counts,
 
 }  // namespace
 
+template <typename E, int KMAX>
+void combine_t(const Dims& m, const void* u, const void* y_r, const void* y_s, const int* perm_slot,
+               const float* gate, void* h, int* status, cudaStream_t st) {
+    const int vecs = m.d * (int)sizeof(E) / 16;                 // 16-byte vectors per row
+    const int threads = vecs >= 256 ? 256 : ((vecs + 31) / 32) * 32;
+    combine_kernel<E, KMAX><<<m.T, threads, 0, st>>>(
+        m, static_cast<const E*>(u), static_cast<const E*>(y_r), static_cast<const E*>(y_s),
+        perm_slot, gate, static_cast<E*>(h), status);
+}
+
 cudaError_t launch_combine(const Dims& m, const void* u, const void* y_r, const void* y_s,
                            const int* perm_slot, const float* gate, void* h, int* status,
                            cudaStream_t st) {
     if (m.T == 0) return cudaSuccess;
-    const int threads = 256, blocks = (m.T + threads / 32 - 1) / (threads / 32);
-    if (m.dtype == MOE_DTYPE_F32)
-        combine_kernel<float><<<blocks, threads, 0, st>>>(
-            m, static_cast<const float*>(u), static_cast<const float*>(y_r),
-            static_cast<const float*>(y_s), perm_slot, gate, static_cast<float*>(h), status);
-    else
-        combine_kernel<__nv_bfloat16><<<blocks, threads, 0, st>>>(
-            m, static_cast<const __nv_bfloat16*>(u), static_cast<const __nv_bfloat16*>(y_r),
-            static_cast<const __nv_bfloat16*>(y_s), perm_slot, gate,
-            static_cast<__nv_bfloat16*>(h), status);
+    if (m.dtype == MOE_DTYPE_F32) {
+        if (m.K <= 4) combine_t<float, 4>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
+        else if (m.K <= 8) combine_t<float, 8>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
+        else combine_t<float, 16>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
+    } else {
+        using B = __nv_bfloat16;
+        if (m.K <= 4) combine_t<B, 4>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
+        else if (m.K <= 8) combine_t<B, 8>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
+        else combine_t<B, 16>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
+    }
     note_launches(1);
     return cudaGetLastError();
 }

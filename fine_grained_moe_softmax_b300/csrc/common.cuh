@@ -121,4 +121,8 @@ __device__ __forceinline__ float silu_f32(float a) { return a / (1.0f + __expf(-
 void note_launches(int n);
 int sm_count();  // multiprocessors of the current device (cached per device)
 
+// Raises the dynamic shared-memory limit of `func` on the current device to at least `bytes`;
+// remembers what each (function, device) was granted so repeated launches skip the call.
+cudaError_t ensure_smem(const void* func, size_t bytes);
+
 }  // namespace moe

@@ -319,8 +319,7 @@ template <int BN, int STAGES, bool GATEUP>
 cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
     using S = Smem<BN, STAGES>;
     auto kern = gemm_tc_kernel<BN, STAGES, GATEUP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)S::total);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), S::total);
     if (e != cudaSuccess) return e;
     const int grid = max(1, min(sm_count(), max_tiles));
     kern<<<grid, kThreads, S::total, st>>>(args);

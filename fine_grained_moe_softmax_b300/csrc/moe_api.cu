@@ -27,6 +27,25 @@ int sm_count() {
     return cached[dev];
 }
 
+cudaError_t ensure_smem(const void* func, size_t bytes) {
+    static std::mutex mu;
+    static std::vector<std::pair<std::pair<const void*, int>, size_t>> granted;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& g : granted)
+        if (g.first.first == func && g.first.second == dev) {
+            if (g.second >= bytes) return cudaSuccess;
+            e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (e == cudaSuccess) g.second = bytes;
+            return e;
+        }
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) granted.push_back({{func, dev}, bytes});
+    return e;
+}
+
 namespace {
 
 int check_cfg(const moe_config* c, Dims* m) {

@@ -244,8 +244,7 @@ cudaError_t launch_perm_scatter(const Dims& m, const int* topk_idx, const int* o
     if (n_tiles == 0) return cudaSuccess;
     const int W = (kRouteTile * m.K + 31) / 32;
     const size_t smem = (size_t)m.N * W * 8 + (size_t)m.N * 4;
-    cudaError_t e = cudaFuncSetAttribute(perm_scatter_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(perm_scatter_kernel), smem);
     if (e != cudaSuccess) return e;
     perm_scatter_kernel<<<n_tiles, 256, smem, st>>>(m, topk_idx, offsets, tile_base, perm_token,
                                                     perm_slot);

@@ -155,8 +155,7 @@ cudaError_t launch_router_t(const Dims& m, const void* u, const void* cent, cons
     const int n_tiles = (m.T + kRouteTile - 1) / kRouteTile;
     const size_t smem = (size_t)kRouteTile * m.N * sizeof(float);
     auto kern = router_simt_kernel<E, KMAX>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     kern<<<n_tiles, kRouterThreads, smem, st>>>(static_cast<const E*>(u),
                                                 static_cast<const E*>(cent), bias, m, idx, gate,

@@ -346,8 +346,7 @@ cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids
                         4 * (4 * kMaxRouted + 2 * kMaxRouted);
     const int n_tiles = (m.T + RBM - 1) / RBM;
     auto kern = m.K <= 8 ? router_tc_kernel<8> : router_tc_kernel<16>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     kern<<<n_tiles, kThreads, smem, st>>>(a);
     note_launches(1);

@@ -68,6 +68,24 @@ class MoELayer:
                             self.losses, self.ws, stream)
         return out
 
+    def capture(self, u: torch.Tensor):
+        """Records one forward on the fixed input buffer ``u`` into a CUDA graph and returns
+        (graph, kernels_per_replay). Replaying the graph reruns the same kernels on the current
+        contents of ``u``, writing the same output buffers; it removes the host-side launch cost,
+        which dominates at decode-sized batches. The call before capture sets up per-device state
+        (tensor-map encoder, shared-memory limits) so that capture records kernels only."""
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self.forward(u)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        torch.cuda.synchronize(self.device)
+        graph = torch.cuda.CUDAGraph()
+        n0 = B.moe_launch_count()
+        with torch.cuda.graph(graph):
+            self.forward(u)
+        return graph, B.moe_launch_count() - n0
+
     def device_status(self, stream=None) -> int:
         return B.moe_device_status(self.ws, stream)
 

@@ -146,3 +146,24 @@ def test_near_tie_threshold_is_rare():
     inputs = moe_inputs.make_inputs(shape, T=4096)
     r = oracle.route(cfg, inputs["u"], inputs["centroids"])
     assert (r["margin"] < NEAR_TIE).sum() <= 8
+
+
+def test_graph_replay_matches_direct_calls():
+    """The layer call captures into a CUDA graph; replays on new contents of the captured input
+    buffer give the same bytes as direct calls."""
+    shape = C["2b_bf16"]
+    inputs = moe_inputs.make_inputs(shape, T=300)
+    layer, u = run_layer(shape, inputs, T=300)
+    graph, kernels = layer.capture(u)
+    assert kernels >= 5
+    u2 = moe_inputs.make_tokens(shape, T=300, seed=99).to("cuda")
+    u.copy_(u2)
+    graph.replay()
+    torch.cuda.synchronize()
+    h_graph, idx_graph, P_graph = layer.h.clone(), layer.topk_idx.clone(), layer.P.clone()
+    layer.forward(u2)
+    torch.cuda.synchronize()
+    assert torch.equal(h_graph, layer.h)
+    assert torch.equal(idx_graph, layer.topk_idx)
+    assert torch.equal(P_graph, layer.P)
+    assert layer.device_status() == 0
