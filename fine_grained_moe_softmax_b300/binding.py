@@ -33,13 +33,15 @@ class MoEConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("n_routed", ctypes.c_int32), ("inter", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("n_groups", ctypes.c_int32),
-                ("alpha1", ctypes.c_float), ("alpha2", ctypes.c_float), ("dtype", ctypes.c_int32)]
+                ("alpha1", ctypes.c_float), ("alpha2", ctypes.c_float), ("dtype", ctypes.c_int32),
+                ("skip_top", ctypes.c_int32), ("drop_shared", ctypes.c_int32)]
 
     @classmethod
     def from_shape(cls, shape, T: Optional[int] = None) -> "MoEConfig":
         return cls(shape.T if T is None else T, shape.d, shape.n_shared, shape.n_routed,
                    shape.inter, shape.top_k, shape.renormalize, shape.n_groups, shape.alpha1,
-                   shape.alpha2, MOE_DTYPE_F32 if shape.dtype == "f32" else MOE_DTYPE_BF16)
+                   shape.alpha2, MOE_DTYPE_F32 if shape.dtype == "f32" else MOE_DTYPE_BF16,
+                   getattr(shape, "skip_top", 0), getattr(shape, "drop_shared", 0))
 
     def torch_dtype(self) -> torch.dtype:
         return torch.float32 if self.dtype == MOE_DTYPE_F32 else torch.bfloat16

@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims m, const E* __restric
                                                       const float* __restrict__ gate,
                                                       E* __restrict__ h, int* status) {
     constexpr int VN = Vec<E>::n;
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     const long TK = (long)m.T * m.K;
     int rows[KMAX];
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims m, const E* __restric
         }
     }
     if (bad && threadIdx.x == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
-    const bool shared = m.Ks > 0;
+    const bool shared = m.shared_active();
     for (int c = threadIdx.x * VN; c < m.d; c += blockDim.x * VN) {
         uint4 raw_u = *reinterpret_cast<const uint4*>(u + (size_t)t * m.d + c);
         uint4 raw_s = shared ? *reinterpret_cast<const uint4*>(y_s + (size_t)t * m.d + c) : raw_u;
@@ -153,9 +155,9 @@ void combine_t(const Dims& m, const void* u, const void* y_r, const void* y_s, c
                const float* gate, void* h, int* status, cudaStream_t st) {
     const int vecs = m.d * (int)sizeof(E) / 16;                 // 16-byte vectors per row
     const int threads = vecs >= 256 ? 256 : ((vecs + 31) / 32) * 32;
-    combine_kernel<E, KMAX><<<m.T, threads, 0, st>>>(
-        m, static_cast<const E*>(u), static_cast<const E*>(y_r), static_cast<const E*>(y_s),
-        perm_slot, gate, static_cast<E*>(h), status);
+    launch_pdl(combine_kernel<E, KMAX>, dim3(m.T), dim3(threads), 0, st, m,
+               static_cast<const E*>(u), static_cast<const E*>(y_r), static_cast<const E*>(y_s),
+               perm_slot, gate, static_cast<E*>(h), status);
 }
 
 cudaError_t launch_combine(const Dims& m, const void* u, const void* y_r, const void* y_s,

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe_b300.h"
 
 namespace moe {
@@ -15,8 +17,11 @@ namespace moe {
 struct Dims {
     int T, d, Ks, N, I, K, renorm, D;
     float a1, a2;
-    int dtype;  // MOE_DTYPE_F32 / MOE_DTYPE_BF16
+    int dtype;        // MOE_DTYPE_F32 / MOE_DTYPE_BF16
+    int skip;         // ablation: disabled top ranks per token (moe_config::skip_top)
+    int drop_shared;  // ablation: shared experts disabled
     __host__ __device__ int elem() const { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
+    __host__ __device__ bool shared_active() const { return Ks > 0 && !drop_shared; }
 };
 
 constexpr int kRouteTile = 128;   // tokens per router / permutation tile
@@ -26,9 +31,9 @@ constexpr int kMaxTopK = 16;      // K' limit
 // Byte offsets of every scratch region inside the caller's workspace (256-byte aligned).
 struct WsLayout {
     size_t status;        // int32 status word (+ padding)
-    size_t tile_counts;   // [n_tiles, N] int32: per router tile, tokens choosing expert j
-    size_t tile_psum;     // [n_tiles, N] fp32: per router tile, sum of affinities
-    size_t tile_base;     // [n_tiles, N] int32: first permuted row of tile's tokens for expert j
+    size_t tile_counts;   // [N, n_tiles] int32: per router tile, tokens choosing expert j
+    size_t tile_psum;     // [N, n_tiles] fp32: per router tile, sum of affinities
+    size_t tile_base;     // [N, n_tiles] int32: first permuted row of tile's tokens for expert j
     size_t psum;          // [N] fp32   (layer forward)
     size_t offsets;       // [N+1] int32 (layer forward)
     size_t perm_token;    // [T*K] int32 (layer forward)
@@ -43,6 +48,9 @@ struct WsLayout {
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Routed experts rounded up to the router's MMA width (a multiple of 32).
+inline int router_npad(const Dims& m) { return (m.N + 31) / 32 * 32; }
 
 inline WsLayout ws_layout(const Dims& m) {
     WsLayout L{};
@@ -115,11 +123,39 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 
 __device__ __forceinline__ float silu_f32(float a) { return a / (1.0f + __expf(-a)); }
 
+// Programmatic dependent launch. Kernels of the layer are launched so that a kernel may start
+// while its predecessor in the stream finishes. pdl_wait() blocks until the predecessor grid has
+// completed and its writes are visible; every kernel calls it before its first global-memory
+// access (read or write) and may do only shared-memory / TMEM / barrier set-up before it.
+// pdl_trigger() lets the successor be scheduled as soon as every CTA of this grid has started.
+// Without a programmatic predecessor both return immediately.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------ host helpers ----
 
 // Counts every kernel launch made through the library (moe_launch_count).
 void note_launches(int n);
 int sm_count();  // multiprocessors of the current device (cached per device)
+
+// Launch with the programmatic-stream-serialization attribute (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Raises the dynamic shared-memory limit of `func` on the current device to at least `bytes`;
 // remembers what each (function, device) was granted so repeated launches skip the call.

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(SimtArgs a) {
     __shared__ float As[SK][SB];
     __shared__ float Bs[SK][SB];
     __shared__ float Us[SK][SB];
+    pdl_wait();
+    pdl_trigger();
     build_tile_prefix<SB>(prefix, rows_s, row0_s, a.offsets, a.gt);
     const int total = prefix[a.gt.n_groups];
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -104,11 +106,12 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(SimtArgs a) {
 template <bool GATEUP>
 cudaError_t run_simt(const Dims& m, SimtArgs a, cudaStream_t st) {
     a.gt.n_groups = 1 + m.N;
-    a.gt.has_shared = m.Ks > 0;
+    a.gt.has_shared = m.shared_active();
     a.gt.T = m.T;
     a.gt.n_tiles_r = (a.n_out_r + SB - 1) / SB;
-    a.gt.n_tiles_s = m.Ks > 0 ? (a.n_out_s + SB - 1) / SB : 0;
-    gemm_simt_kernel<GATEUP><<<4 * sm_count(), 256, 0, st>>>(a);
+    a.gt.n_tiles_s = m.shared_active() ? (a.n_out_s + SB - 1) / SB : 0;
+    cudaError_t e = launch_pdl(gemm_simt_kernel<GATEUP>, dim3(4 * sm_count()), dim3(256), 0, st, a);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
 }

@@ -144,6 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         ptx::tmem_alloc(ptx::smem_addr(tmem_holder), 2 * BN);
         ptx::tmem_relinquish();
     }
+    pdl_wait();
+    pdl_trigger();
     build_tile_prefix<BM>(prefix, rows_s, row0_s, args.offsets, gt);   // contains __syncthreads
     ptx::tc_fence_before();
     __syncthreads();
@@ -322,7 +324,8 @@ cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), S::total);
     if (e != cudaSuccess) return e;
     const int grid = max(1, min(sm_count(), max_tiles));
-    kern<<<grid, kThreads, S::total, st>>>(args);
+    e = launch_pdl(kern, dim3(grid), dim3(kThreads), S::total, st, args);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
 }
@@ -339,7 +342,7 @@ struct GemmShape {
 template <bool GATEUP>
 cudaError_t run_gemm(const Dims& m, const GemmShape& g, const int* offsets, int* status,
                      cudaStream_t st) {
-    const bool shared = m.Ks > 0;
+    const bool shared = m.shared_active();
     const int bn = (g.n_cols_r % 256 == 0 && (!shared || g.n_cols_s % 256 == 0)) ? 256 : 128;
     TcArgs a{};
     if (!encode_bf16_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, BM) ||

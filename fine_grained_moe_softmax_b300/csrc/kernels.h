@@ -10,7 +10,8 @@
 
 namespace moe {
 
-// Router: per 128-token tile, logits, softmax, top-k, gates, tile histogram and affinity sums.
+// Router: per 128-token tile, logits, softmax, top-k, gates, tile histogram and affinity sums
+// (tables expert-major: [N][n_tiles]).
 cudaError_t launch_router(const Dims& m, const void* u, const void* centroids, const float* bias,
                           int* topk_idx, float* topk_gate, int* tile_counts, float* tile_psum,
                           int* status, cudaStream_t st);

@@ -53,9 +53,11 @@ int check_cfg(const moe_config* c, Dims* m) {
     if (c->T < 0 || c->d <= 0 || c->n_shared < 0 || c->n_routed <= 0 || c->inter <= 0 ||
         c->top_k <= 0 || c->top_k > c->n_routed || c->n_groups <= 0 ||
         c->n_groups > c->n_routed || (c->renormalize != 0 && c->renormalize != 1) ||
-        (c->dtype != MOE_DTYPE_F32 && c->dtype != MOE_DTYPE_BF16))
+        (c->dtype != MOE_DTYPE_F32 && c->dtype != MOE_DTYPE_BF16) || c->skip_top < 0 ||
+        c->skip_top + c->top_k > c->n_routed || (c->drop_shared != 0 && c->drop_shared != 1))
         return MOE_ERR_INVALID_ARG;
-    if (c->d % 64 != 0 || c->inter % 16 != 0 || c->n_routed > kMaxRouted || c->top_k > kMaxTopK)
+    if (c->d % 64 != 0 || c->inter % 16 != 0 || c->n_routed > kMaxRouted ||
+        c->skip_top + c->top_k > kMaxTopK)
         return MOE_ERR_UNSUPPORTED;
     // row indices and element counts stay inside int32 / the tensor-map limits
     const long long TK = (long long)c->T * c->top_k;
@@ -74,6 +76,8 @@ int check_cfg(const moe_config* c, Dims* m) {
     m->a1 = c->alpha1;
     m->a2 = c->alpha2;
     m->dtype = c->dtype;
+    m->skip = c->skip_top;
+    m->drop_shared = c->drop_shared;
     return MOE_OK;
 }
 
@@ -224,7 +228,7 @@ int moe_expert_ffn(const moe_config* cfg, const void* u, const void* packed_w,
     if (rc != MOE_OK) return rc;
     if (!packed_w || !aligned16(packed_w) || !offsets ||
         (m.T > 0 && (!u || !aligned16(u) || !perm_token || !y_routed || !aligned16(y_routed) ||
-                     (m.Ks > 0 && (!y_shared || !aligned16(y_shared))))))
+                     (m.shared_active() && (!y_shared || !aligned16(y_shared))))))
         return MOE_ERR_INVALID_ARG;
     if ((rc = check_ws(m, ws, ws_bytes)) != MOE_OK) return rc;
     const WsLayout L = ws_layout(m);
@@ -247,7 +251,7 @@ int moe_combine(const moe_config* cfg, const void* u, const void* y_routed, cons
     int rc = check_cfg(cfg, &m);
     if (rc != MOE_OK) return rc;
     if (m.T > 0 && (!u || !y_routed || !perm_slot || !topk_gate || !h || !aligned16(u) ||
-                    !aligned16(y_routed) || !aligned16(h) || (m.Ks > 0 && !y_shared) ||
+                    !aligned16(y_routed) || !aligned16(h) || (m.shared_active() && !y_shared) ||
                     (y_shared && !aligned16(y_shared))))
         return MOE_ERR_INVALID_ARG;
     if ((rc = check_ws(m, ws, ws_bytes)) != MOE_OK) return rc;

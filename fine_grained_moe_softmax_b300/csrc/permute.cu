@@ -30,36 +30,52 @@ __global__ void tile_hist_kernel(Dims m, const int* __restrict__ topk_idx,
     if (bad) set_status(status, MOE_ERR_CORRUPT_INPUT);
     __syncthreads();
     for (int j = threadIdx.x; j < m.N; j += blockDim.x)
-        tile_counts[(size_t)tile * m.N + j] = hist[j];
+        tile_counts[(size_t)j * gridDim.x + tile] = hist[j];
 }
 
-// One CTA of 32 warps. Warp w handles experts w, w+32, ...: its lanes walk the tiles 32 at a time
-// (tile = chunk + lane), a warp scan gives each tile's base inside the expert (token order), and a
-// fixed-pattern butterfly sums the tile affinity sums, so the result is the same on every run.
+// One CTA of 32 warps. Warp w handles experts w, w+32, ...: its lanes walk the expert's row of the
+// per-tile tables ([N][n_tiles], expert-major) 32 tiles at a time, a warp scan gives each tile's
+// base inside the expert (token order), and a fixed-pattern butterfly sums the tile affinity
+// sums, so the result is the same on every run.
 // Optional outputs: counts / psum (router totals), offsets (exclusive scan over experts), the
 // balance statistics, and a check of the totals against caller-supplied counts.
 __global__ void __launch_bounds__(1024) route_finalize_kernel(FinalizeArgs a) {
     __shared__ int total[kMaxRouted];
     __shared__ float ptot[kMaxRouted];
     __shared__ int off[kMaxRouted + 1];
+    pdl_wait();
+    pdl_trigger();
     const Dims m = a.m;
     const int N = m.N, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int j = warp; j < N; j += 32) {
+        const int* cnt = a.tile_counts + (size_t)j * a.n_tiles;
+        const float* ps = a.tile_psum ? a.tile_psum + (size_t)j * a.n_tiles : nullptr;
+        int* tb = a.tile_base ? a.tile_base + (size_t)j * a.n_tiles : nullptr;
         int carry = 0;
         float p = 0.f;
-        for (int c0 = 0; c0 < a.n_tiles; c0 += 32) {
-            const int tile = c0 + lane;
-            const bool in = tile < a.n_tiles;
-            const int c = in ? a.tile_counts[(size_t)tile * N + j] : 0;
-            int incl = c;
+        for (int c0 = 0; c0 < a.n_tiles; c0 += 4 * 32) {   // loads of four chunks first
+            int cv[4];
+            float pv[4];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
+            for (int q = 0; q < 4; ++q) {
+                const int tile = c0 + q * 32 + lane;
+                const bool in = tile < a.n_tiles;
+                cv[q] = in ? cnt[tile] : 0;
+                pv[q] = (ps && in) ? ps[tile] : 0.f;
             }
-            if (a.tile_base && in) a.tile_base[(size_t)tile * N + j] = carry + incl - c;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-            if (a.tile_psum && in) p += a.tile_psum[(size_t)tile * N + j];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int tile = c0 + q * 32 + lane;
+                int incl = cv[q];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                if (tb && tile < a.n_tiles) tb[tile] = carry + incl - cv[q];
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+                p += pv[q];
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
@@ -130,9 +146,11 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(Dims m, const int* __
     int* base = pre + (size_t)N * W;                            // [N]
     const int tile = blockIdx.x, t0 = tile * kRouteTile;
     const int n = min(kRouteTile, m.T - t0) * K;
+    pdl_wait();
+    pdl_trigger();
     for (int i = threadIdx.x; i < N * W; i += blockDim.x) bits[i] = 0u;
     for (int j = threadIdx.x; j < N; j += blockDim.x)
-        base[j] = offsets[j] + tile_base[(size_t)tile * N + j];
+        base[j] = offsets[j] + tile_base[(size_t)j * gridDim.x + tile];
     __syncthreads();
     const int* idx = topk_idx + (size_t)t0 * K;
     for (int a = threadIdx.x; a < n; a += blockDim.x) {
@@ -166,6 +184,8 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(Dims m, const int* __
 // One warp per token: the row is read once (16-byte vectors) and written to its K' rows.
 __global__ void gather_kernel(Dims m, const uint4* __restrict__ u, const int* __restrict__ perm_slot,
                               uint4* __restrict__ x_perm, int* status) {
+    pdl_wait();
+    pdl_trigger();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= m.T) return;
     const int vec_per_row = m.d * m.elem() / 16;
@@ -232,7 +252,8 @@ cudaError_t launch_tile_hist(const Dims& m, const int* topk_idx, int* tile_count
 }
 
 cudaError_t launch_route_finalize(const FinalizeArgs& a, cudaStream_t st) {
-    route_finalize_kernel<<<1, 1024, 0, st>>>(a);
+    cudaError_t e = launch_pdl(route_finalize_kernel, dim3(1), dim3(1024), 0, st, a);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
 }
@@ -246,8 +267,9 @@ cudaError_t launch_perm_scatter(const Dims& m, const int* topk_idx, const int* o
     const size_t smem = (size_t)m.N * W * 8 + (size_t)m.N * 4;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(perm_scatter_kernel), smem);
     if (e != cudaSuccess) return e;
-    perm_scatter_kernel<<<n_tiles, 256, smem, st>>>(m, topk_idx, offsets, tile_base, perm_token,
-                                                    perm_slot);
+    e = launch_pdl(perm_scatter_kernel, dim3(n_tiles), dim3(256), smem, st, m, topk_idx, offsets,
+                   tile_base, perm_token, perm_slot);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
 }
@@ -257,8 +279,10 @@ cudaError_t launch_gather(const Dims& m, const void* u, const int* perm_slot, vo
     if (m.T == 0) return cudaSuccess;
     const int threads = 256, warps_per_block = threads / 32;
     const int blocks = (m.T + warps_per_block - 1) / warps_per_block;
-    gather_kernel<<<blocks, threads, 0, st>>>(m, static_cast<const uint4*>(u), perm_slot,
-                                              static_cast<uint4*>(x_perm), status);
+    cudaError_t e = launch_pdl(gather_kernel, dim3(blocks), dim3(threads), 0, st, m,
+                               static_cast<const uint4*>(u), perm_slot,
+                               static_cast<uint4*>(x_perm), status);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
 }

@@ -76,6 +76,8 @@ router_simt_kernel(const E* __restrict__ u, const E* __restrict__ cent,
     const int tile = blockIdx.x, t0 = tile * kRouteTile;
     const int n_tok = min(kRouteTile, m.T - t0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     for (int j = threadIdx.x; j < N; j += blockDim.x) hist[j] = 0;
 
     for (int tl = warp; tl < n_tok; tl += kRouterThreads / 32) {
@@ -120,19 +122,20 @@ router_simt_kernel(const E* __restrict__ u, const E* __restrict__ cent,
         }
         const float inv = 1.0f / sum;
         for (int j = 0; j < N; ++j) z[j] = expf(z[j] - zmax) * inv;   // z row now holds s
+        const int q0 = m.skip;   // chosen ranks: q0 .. q0+K'-1
         float gsum = 0.f;
 #pragma unroll
         for (int q = 0; q < KMAX; ++q)
-            if (q < K) gsum += expf(top.v[q] - zmax) * inv;
+            if (q >= q0 && q < q0 + K) gsum += expf(top.v[q] - zmax) * inv;
         bool bad = !(zmax < INFINITY);
 #pragma unroll
         for (int q = 0; q < KMAX; ++q) {
-            if (q < K) {
+            if (q >= q0 && q < q0 + K) {
                 int j = top.i[q];
                 if (j < 0) { bad = true; j = 0; }
                 const float s = expf(top.v[q] - zmax) * inv;
-                topk_idx[(size_t)t * K + q] = j;
-                topk_gate[(size_t)t * K + q] = m.renorm ? s / gsum : s;
+                topk_idx[(size_t)t * K + q - q0] = j;
+                topk_gate[(size_t)t * K + q - q0] = m.renorm ? s / gsum : s;
                 atomicAdd(&hist[j], 1);
             }
         }
@@ -143,8 +146,8 @@ router_simt_kernel(const E* __restrict__ u, const E* __restrict__ cent,
     for (int j = threadIdx.x; j < N; j += blockDim.x) {
         float acc = 0.f;
         for (int tl = 0; tl < n_tok; ++tl) acc += z_s[tl * N + j];
-        tile_psum[(size_t)tile * N + j] = acc;
-        tile_counts[(size_t)tile * N + j] = hist[j];
+        tile_psum[(size_t)j * gridDim.x + tile] = acc;
+        tile_counts[(size_t)j * gridDim.x + tile] = hist[j];
     }
 }
 
@@ -157,9 +160,9 @@ cudaError_t launch_router_t(const Dims& m, const void* u, const void* cent, cons
     auto kern = router_simt_kernel<E, KMAX>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    kern<<<n_tiles, kRouterThreads, smem, st>>>(static_cast<const E*>(u),
-                                                static_cast<const E*>(cent), bias, m, idx, gate,
-                                                tc, tp, status);
+    e = launch_pdl(kern, dim3(n_tiles), dim3(kRouterThreads), smem, st, static_cast<const E*>(u),
+                   static_cast<const E*>(cent), bias, m, idx, gate, tc, tp, status);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
 }
@@ -173,7 +176,7 @@ cudaError_t launch_router(const Dims& m, const void* u, const void* centroids, c
     if (m.dtype == MOE_DTYPE_BF16)
         return launch_router_tc(m, u, centroids, bias, topk_idx, topk_gate, tile_counts,
                                 tile_psum, status, st);
-    return m.K <= 8 ? launch_router_t<float, 8>(m, u, centroids, bias, topk_idx, topk_gate,
+    return m.skip + m.K <= 8 ? launch_router_t<float, 8>(m, u, centroids, bias, topk_idx, topk_gate,
                                                 tile_counts, tile_psum, status, st)
                     : launch_router_t<float, 16>(m, u, centroids, bias, topk_idx, topk_gate,
                                                  tile_counts, tile_psum, status, st);

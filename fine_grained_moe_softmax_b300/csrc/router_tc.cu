@@ -8,10 +8,10 @@
 // The logits of a 128-token tile are one [128 x d] x [d x N'] product: the tile's token rows and
 // the centroids stream through a TMA ring into tcgen05.mma (M = 128, N = N' rounded up to 32),
 // accumulating fp32 logits in TMEM. Four epilogue warps then own one token per thread: each reads
-// its logit row from TMEM (warp w sees TMEM lanes 32*(w%4) .. +31), adds the optional bias, and
-// computes the softmax, a register top-K' (ranked by logit; the lower index wins ties), the gates,
-// the tile's expert histogram and, by a warp transpose-reduction, the tile's per-expert sums of
-// affinities in a fixed order.
+// its logit row from TMEM once (warp w sees TMEM lanes 32*(w%4) .. +31), adds the optional bias,
+// keeps the row in the (by then idle) TMA ring, and computes the softmax, a register top-K'
+// (ranked by logit; the lower index wins ties), the gates, the tile's expert histogram and, by a
+// warp transpose-reduction, the tile's per-expert sums of affinities in a fixed order.
 #include <math.h>
 
 #include "common.cuh"
@@ -32,7 +32,7 @@ struct RouterArgs {
     CUtensorMap a;        // u [T, d], box [128 x 64]
     CUtensorMap b;        // centroids [N', d], box [n_pad x 64]
     const float* bias;    // [N'] or null
-    int T, N, K, renorm, k_blocks, n_pad, stages, tmem_cols;
+    int T, N, K, renorm, skip, k_blocks, n_pad, stages, tmem_cols;
     uint32_t stage_bytes;
     int* topk_idx;
     float* topk_gate;
@@ -100,6 +100,83 @@ __device__ __forceinline__ void epilogue_bar() {
     asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// Routing of the 128 tokens of a tile by the four epilogue warps (thread = token): softmax over
+// the N' routed experts, top-K' by logit (lower index on ties), gates, the tile histogram and the
+// tile's per-expert affinity sums. `zc` ([n_pad][128] floats, column j of row r at j * 128 + r,
+// conflict-free per warp) receives the biased logits and then the exponentials, so TMEM is read
+// once and every exponential is computed once.
+template <int KMAX>
+__device__ __forceinline__ void route_tile(const RouterArgs& a, uint32_t tmem_lanes, float* zc,
+                                          int tile, int quarter, int lane, float* colsum,
+                                          int* hist, const float* bias_s) {
+    const int N = a.N, K = a.K;
+    const int row = quarter * 32 + lane;
+    const int t = tile * RBM + row;
+    const bool valid = t < a.T;
+    const int n_chunks = a.n_pad / 32;
+    // pass 1 (TMEM): biased logits, their maximum and the top list
+    float zmax = -INFINITY;
+    TopK<KMAX> top;
+    top.init();
+    for (int c = 0; c < n_chunks; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tmem_lanes + c * 32, v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int j = c * 32 + i;
+            if (j < N) {
+                const float z = __uint_as_float(v[i]) + bias_s[j];
+                zc[j * RBM + row] = z;
+                zmax = fmaxf(zmax, z);
+                top.push(z, j);
+            }
+        }
+    }
+    // pass 2: exponentials and the softmax denominator
+    float sum = 0.f;
+    for (int j = 0; j < N; ++j) {
+        const float e = __expf(zc[j * RBM + row] - zmax);
+        zc[j * RBM + row] = e;
+        sum += e;
+    }
+    const float inv = 1.0f / sum;
+    if (valid) {
+        const int q0 = a.skip;   // chosen ranks: q0 .. q0+K'-1
+        float gsum = 0.f;
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q)
+            if (q >= q0 && q < q0 + K) gsum += __expf(top.v[q] - zmax) * inv;
+        bool bad = !(zmax < INFINITY);
+#pragma unroll
+        for (int q = 0; q < KMAX; ++q) {
+            if (q >= q0 && q < q0 + K) {
+                int j = top.i[q];
+                if (j < 0) {
+                    bad = true;
+                    j = 0;
+                }
+                const float s = __expf(top.v[q] - zmax) * inv;
+                a.topk_idx[(size_t)t * K + q - q0] = j;
+                a.topk_gate[(size_t)t * K + q - q0] = a.renorm ? s / gsum : s;
+                atomicAdd(&hist[j], 1);
+            }
+        }
+        if (bad) set_status(a.status, MOE_ERR_CORRUPT_INPUT);
+    }
+    // pass 3: affinities, summed over this warp's 32 tokens per expert column
+    for (int c = 0; c < n_chunks; ++c) {
+        float s[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int j = c * 32 + i;
+            s[i] = (valid && j < N) ? zc[j * RBM + row] * inv : 0.f;
+        }
+        const float col = column_sums(s, lane);
+        colsum[quarter * kMaxRouted + c * 32 + lane] = col;
+    }
+}
+
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_constant__ RouterArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -118,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x;
-    const int N = a.N, K = a.K;
+    const int N = a.N;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -130,10 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
-    for (int j = threadIdx.x; j < kMaxRouted; j += blockDim.x) {
-        hist[j] = 0;
-        bias_s[j] = (a.bias && j < N) ? a.bias[j] : 0.f;
-    }
+    for (int j = threadIdx.x; j < kMaxRouted; j += blockDim.x) hist[j] = 0;
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&a.a);
         ptx::prefetch_tmap(&a.b);
@@ -142,6 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
         ptx::tmem_alloc(ptx::smem_addr(tmem_holder), a.tmem_cols);
         ptx::tmem_relinquish();
     }
+    pdl_wait();
+    pdl_trigger();
+    for (int j = threadIdx.x; j < kMaxRouted; j += blockDim.x)
+        bias_s[j] = (a.bias && j < N) ? a.bias[j] : 0.f;
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -216,94 +294,28 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     } else {
         // --------------------------------------------------------------------- epilogue ----
         const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
-        const int t = tile * RBM + row;
-        const bool valid = t < a.T;
+        const int et = threadIdx.x - 64;   // 0..127 over the four epilogue warps
         int ok = 1;
         if (lane == 0) ok = wait_phase(ptx::smem_addr(tfull), 0, abort_flag, a.status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        const int n_chunks = a.n_pad / 32;
+        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16);
+        bool routed_here = false;
         if (ok) {
             ptx::tc_fence_after();
-            const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16);
-            // pass 1: largest logit and the top-K' list
-            float zmax = -INFINITY;
-            TopK<KMAX> top;
-            top.init();
-            for (int c = 0; c < n_chunks; ++c) {
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(tb + c * 32, v);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = c * 32 + i;
-                    if (j < N) {
-                        const float z = __uint_as_float(v[i]) + bias_s[j];
-                        zmax = fmaxf(zmax, z);
-                        top.push(z, j);
-                    }
-                }
-            }
-            // pass 2: softmax denominator
-            float sum = 0.f;
-            for (int c = 0; c < n_chunks; ++c) {
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(tb + c * 32, v);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = c * 32 + i;
-                    if (j < N) sum += expf(__uint_as_float(v[i]) + bias_s[j] - zmax);
-                }
-            }
-            const float inv = 1.0f / sum;
-            if (valid) {
-                float gsum = 0.f;
-#pragma unroll
-                for (int q = 0; q < KMAX; ++q)
-                    if (q < K) gsum += expf(top.v[q] - zmax) * inv;
-                bool bad = !(zmax < INFINITY);
-#pragma unroll
-                for (int q = 0; q < KMAX; ++q) {
-                    if (q < K) {
-                        int j = top.i[q];
-                        if (j < 0) {
-                            bad = true;
-                            j = 0;
-                        }
-                        const float s = expf(top.v[q] - zmax) * inv;
-                        a.topk_idx[(size_t)t * K + q] = j;
-                        a.topk_gate[(size_t)t * K + q] = a.renorm ? s / gsum : s;
-                        atomicAdd(&hist[j], 1);
-                    }
-                }
-                if (bad) set_status(a.status, MOE_ERR_CORRUPT_INPUT);
-            }
-            // pass 3: affinities, summed over this warp's 32 tokens per expert column
-            for (int c = 0; c < n_chunks; ++c) {
-                uint32_t v[32];
-                ptx::tmem_ld_32x32b_x32(tb + c * 32, v);
-                ptx::tmem_ld_wait();
-                float s[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = c * 32 + i;
-                    s[i] = (valid && j < N) ? expf(__uint_as_float(v[i]) + bias_s[j] - zmax) * inv
-                                            : 0.f;
-                }
-                const float col = column_sums(s, lane);
-                colsum[quarter * kMaxRouted + c * 32 + lane] = col;
-            }
+            // the MMAs are complete, so the TMA ring is idle and holds the per-token logit rows
+            route_tile<KMAX>(a, tb, reinterpret_cast<float*>(base), tile, quarter, lane, colsum,
+                             hist, bias_s);
+            routed_here = true;
         }
         ptx::tc_fence_before();
         epilogue_bar();
-        if (ok) {
-            const int et = threadIdx.x - 64;   // 0..127 over the four epilogue warps
+        if (routed_here) {
+            const int n_tiles = gridDim.x;
             for (int j = et; j < N; j += 128) {
-                a.tile_psum[(size_t)tile * N + j] =
+                a.tile_psum[(size_t)j * n_tiles + tile] =
                     ((colsum[j] + colsum[kMaxRouted + j]) + colsum[2 * kMaxRouted + j]) +
                     colsum[3 * kMaxRouted + j];
-                a.tile_counts[(size_t)tile * N + j] = hist[j];
+                a.tile_counts[(size_t)j * n_tiles + tile] = hist[j];
             }
         }
     }
@@ -322,7 +334,7 @@ cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids
                              const float* bias, int* topk_idx, float* topk_gate, int* tile_counts,
                              float* tile_psum, int* status, cudaStream_t st) {
     RouterArgs a{};
-    a.n_pad = (m.N + 31) / 32 * 32;
+    a.n_pad = router_npad(m);
     if (!encode_bf16_map(&a.a, u, (uint64_t)m.T, (uint64_t)m.d, RBM) ||
         !encode_bf16_map(&a.b, centroids, (uint64_t)m.N, (uint64_t)m.d, a.n_pad))
         return cudaErrorInvalidValue;
@@ -331,6 +343,7 @@ cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids
     a.N = m.N;
     a.K = m.K;
     a.renorm = m.renorm;
+    a.skip = m.skip;
     a.k_blocks = m.d / RBK;
     a.stage_bytes = (uint32_t)(RBM * RBK * 2 + a.n_pad * RBK * 2);
     a.stages = (int)std::min<uint32_t>(kMaxStages, (192u * 1024u) / a.stage_bytes);
@@ -345,10 +358,11 @@ cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids
     const size_t smem = 1024 + (size_t)a.stages * a.stage_bytes + 8 * (2 * kMaxStages + 2) + 16 +
                         4 * (4 * kMaxRouted + 2 * kMaxRouted);
     const int n_tiles = (m.T + RBM - 1) / RBM;
-    auto kern = m.K <= 8 ? router_tc_kernel<8> : router_tc_kernel<16>;
+    auto kern = m.skip + m.K <= 8 ? router_tc_kernel<8> : router_tc_kernel<16>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    kern<<<n_tiles, kThreads, smem, st>>>(a);
+    e = launch_pdl(kern, dim3(n_tiles), dim3(kThreads), smem, st, a);
+    if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
 }

@@ -23,9 +23,9 @@
  *     The return value reports argument and launch errors only. Errors found on the device
  *     (a bounded wait that ran out, corrupt routing input) are written to a status word inside
  *     `ws`; each call clears that word when it starts, and moe_device_status() reads it.
- *   - Supported shapes: T >= 0, d % 64 == 0, I % 16 == 0, 1 <= top_k <= min(N', 16),
- *     1 <= N' <= 256, 0 <= K_s, 1 <= n_groups <= N'. Anything else returns
- *     MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED; there is no fallback path.
+ *   - Supported shapes: T >= 0, d % 64 == 0, I % 16 == 0, 1 <= top_k, skip_top >= 0,
+ *     skip_top + top_k <= min(N', 16), 1 <= N' <= 256, 0 <= K_s, 1 <= n_groups <= N'. Anything
+ *     else returns MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED; there is no fallback path.
  *   - Calls on different streams with disjoint workspaces and outputs are independent.
  */
 #ifndef MOE_B300_H
@@ -64,6 +64,11 @@ typedef struct {
     float alpha1;        /* expert-level balance factor */
     float alpha2;        /* device-level balance factor */
     int32_t dtype;       /* moe_dtype of u, h, centroids and weights */
+    /* Ablations of the expert-specialisation analysis ([P1] §专家特化深度分析); 0 = the layer. */
+    int32_t skip_top;    /* the skip_top best-ranked routed experts of each token are disabled:
+                          * the token uses ranks skip_top .. skip_top+K'-1, gates = their s */
+    int32_t drop_shared; /* 1: the shared experts are disabled (no shared term in h; moe_expert_ffn
+                          * leaves y_shared untouched) */
 } moe_config;
 
 /* Bytes of scratch any entry point may use for this configuration (the same figure for all). */

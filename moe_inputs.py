@@ -46,6 +46,8 @@ class MoEShape:
     alpha2: float = 0.05
     renormalize: int = 0
     zipf_s: Optional[float] = None   # logit bias -zipf_s*ln(rank) per routed expert
+    skip_top: int = 0                # ablation: disable each token's skip_top best routed experts
+    drop_shared: int = 0             # ablation: disable the shared experts
     description: str = ""
 
     @property
@@ -75,6 +77,15 @@ CONFIGS = {
         "16b_decode_bf16", T=64, d=2048, n_shared=2, n_routed=64, inter=1408, top_k=6,
         n_groups=8, dtype="bf16", seed=3,
         description="16B-like decode step: batch 64 x 1 token (weight-bandwidth bound)"),
+    # the pages' analysis variants (section 专家特化深度分析 and the coarse baseline of Fig. 2(a))
+    "2b_half_activated_bf16": MoEShape(
+        "2b_half_activated_bf16", T=8192, d=1280, n_shared=1, n_routed=63, inter=320, top_k=3,
+        n_groups=8, dtype="bf16", seed=5,
+        description="2B-like layer with half the activated experts: 1 shared + top-3 routed"),
+    "2b_gshard_top2_bf16": MoEShape(
+        "2b_gshard_top2_bf16", T=8192, d=1280, n_shared=0, n_routed=16, inter=1280, top_k=2,
+        n_groups=8, dtype="bf16", seed=6,
+        description="coarse top-2 baseline (m = 1, no shared expert): 16 experts of width 4*320"),
     "145b_zipf_bf16": MoEShape(
         "145b_zipf_bf16", T=8192, d=4096, n_shared=4, n_routed=128, inter=1536, top_k=12,
         n_groups=8, dtype="bf16", seed=4, zipf_s=1.1,

@@ -35,6 +35,10 @@
  *   - f_j = N'/(K' T) count_j, P_j = (1/T) sum_t s_{t,j}; groups are contiguous routed-id ranges,
  *     the first (N' mod D) groups one expert larger; f'_g = mean of f over the group, P'_g = sum
  *     of P over the group.
+ *   - ablations of "DeepSeekMoE 论文解读" §专家特化深度分析: disabling a token's top routed
+ *     experts (skip_top = r) routes it to the experts ranked r+1 .. r+K' with their own affinities
+ *     as gates (the softmax is unchanged); disabling the shared experts (drop_shared) removes
+ *     their term from h.
  */
 #include <math.h>
 #include <stdint.h>
@@ -49,7 +53,9 @@ enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
 typedef struct {
     int T, d, n_shared, n_routed, inter, top_k, renormalize, n_groups;
     double alpha1, alpha2;
-    int dtype; /* ORACLE_F32: float values; ORACLE_BF16: uint16 bf16 bit patterns */
+    int dtype;       /* ORACLE_F32: float values; ORACLE_BF16: uint16 bf16 bit patterns */
+    int skip_top;    /* ablation: the skip_top best-ranked routed experts of a token are disabled */
+    int drop_shared; /* ablation: 1 = the shared experts are disabled */
 } oracle_cfg;
 
 /* Exact widening of element i of an fp32 or bf16 array to double. A bf16 value is the upper
@@ -104,19 +110,22 @@ static void rank_experts(const double* s, int N, int* order) {
 void oracle_token_route(const oracle_cfg* c, const void* u, const void* centroids,
                         const float* bias, int t, double* s, int32_t* idx, double* gate,
                         double* margin) {
-    const int N = c->n_routed, K = c->top_k;
+    const int N = c->n_routed, K = c->top_k, r0 = c->skip_top;
     int* order = (int*)malloc(sizeof(int) * (size_t)N);
     token_affinity(c, u, centroids, bias, t, s);
     rank_experts(s, N, order);
     double topsum = 0.0;
-    for (int k = 0; k < K; ++k) topsum += s[order[k]];
+    for (int k = 0; k < K; ++k) topsum += s[order[r0 + k]];
     for (int k = 0; k < K; ++k) {
-        idx[k] = order[k];
-        gate[k] = c->renormalize ? s[order[k]] / topsum : s[order[k]];
+        idx[k] = order[r0 + k];
+        gate[k] = c->renormalize ? s[order[r0 + k]] / topsum : s[order[r0 + k]];
     }
+    /* the chosen ranks are r0 .. r0+K-1: every neighbouring pair from rank r0-1 to r0+K decides
+     * the set or its order */
     double m = INFINITY;
-    int last = (K < N) ? K : K - 1;
-    for (int r = 0; r < last; ++r) {
+    const int first = r0 > 0 ? r0 - 1 : 0;
+    const int last = (r0 + K < N) ? r0 + K : N - 1;
+    for (int r = first; r < last; ++r) {
         double gap = s[order[r]] - s[order[r + 1]];
         if (gap < m) m = gap;
     }
@@ -131,7 +140,7 @@ int oracle_route(const oracle_cfg* c, const void* u, const void* centroids, cons
                  int32_t* topk_idx, double* topk_gate, double* margin, int64_t* counts,
                  double* psum, double* scores) {
     const int T = c->T, N = c->n_routed, K = c->top_k;
-    if (T < 0 || N < 1 || K < 1 || K > N) return -1;
+    if (T < 0 || N < 1 || K < 1 || c->skip_top < 0 || c->skip_top + K > N) return -1;
     double* all_s = scores ? scores : (double*)malloc(sizeof(double) * (size_t)T * N + 1);
 #pragma omp parallel for schedule(dynamic, 16)
     for (int t = 0; t < T; ++t)
@@ -218,6 +227,8 @@ int oracle_forward_tokens(const oracle_cfg* c, const void* u, const void* centro
     const int d = c->d, N = c->n_routed, K = c->top_k, Ks = c->n_shared;
     for (int q = 0; q < n; ++q)
         if (tokens[q] < 0 || tokens[q] >= c->T) return -1;
+    if (c->skip_top < 0 || c->skip_top + K > N) return -1;
+    const int n_active_shared = c->drop_shared ? 0 : Ks;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int q = 0; q < n; ++q) {
         const int t = tokens[q];
@@ -233,7 +244,7 @@ int oracle_forward_tokens(const oracle_cfg* c, const void* u, const void* centro
         for (int k = 0; k < d; ++k) hq[k] = x[k];
         if (shared_out)
             for (int k = 0; k < d; ++k) shared_out[(size_t)q * d + k] = 0.0;
-        for (int e = 0; e < Ks; ++e) {
+        for (int e = 0; e < n_active_shared; ++e) {
             oracle_expert_ffn(c, w_gate, w_up, w_down, e, x, y);
             for (int k = 0; k < d; ++k) hq[k] += y[k];
             if (shared_out)

@@ -40,7 +40,8 @@ class _Cfg(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("n_shared", ctypes.c_int),
                 ("n_routed", ctypes.c_int), ("inter", ctypes.c_int), ("top_k", ctypes.c_int),
                 ("renormalize", ctypes.c_int), ("n_groups", ctypes.c_int),
-                ("alpha1", ctypes.c_double), ("alpha2", ctypes.c_double), ("dtype", ctypes.c_int)]
+                ("alpha1", ctypes.c_double), ("alpha2", ctypes.c_double), ("dtype", ctypes.c_int),
+                ("skip_top", ctypes.c_int), ("drop_shared", ctypes.c_int)]
 
 
 @dataclass
@@ -56,18 +57,22 @@ class OracleCfg:
     alpha1: float = 0.01
     alpha2: float = 0.05
     dtype: str = "f32"
+    skip_top: int = 0
+    drop_shared: int = 0
 
     @classmethod
     def from_shape(cls, shape, T: Optional[int] = None) -> "OracleCfg":
         return cls(T=shape.T if T is None else T, d=shape.d, n_shared=shape.n_shared,
                    n_routed=shape.n_routed, inter=shape.inter, top_k=shape.top_k,
                    renormalize=shape.renormalize, n_groups=shape.n_groups, alpha1=shape.alpha1,
-                   alpha2=shape.alpha2, dtype=shape.dtype)
+                   alpha2=shape.alpha2, dtype=shape.dtype,
+                   skip_top=getattr(shape, "skip_top", 0),
+                   drop_shared=getattr(shape, "drop_shared", 0))
 
     def c(self) -> _Cfg:
         return _Cfg(self.T, self.d, self.n_shared, self.n_routed, self.inter, self.top_k,
                     self.renormalize, self.n_groups, self.alpha1, self.alpha2,
-                    F32 if self.dtype == "f32" else BF16)
+                    F32 if self.dtype == "f32" else BF16, self.skip_top, self.drop_shared)
 
 
 def _load():

@@ -69,6 +69,8 @@ def _cfg(**kw):
     (dict(n_groups=0), -1), (dict(renormalize=2), -1), (dict(dtype=7), -1),
     (dict(n_routed=0), -1), (dict(d=96), -2), (dict(inter=24), -2),
     (dict(n_routed=300, n_groups=2), -2), (dict(n_routed=64, top_k=17), -2),
+    (dict(skip_top=-1), -1), (dict(skip_top=7), -1), (dict(drop_shared=2), -1),
+    (dict(n_routed=64, top_k=8, skip_top=9), -2),
 ])
 def test_config_validation(lib, kw, code):
     cfg = _cfg(**kw)

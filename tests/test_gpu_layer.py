@@ -47,7 +47,8 @@ def _compare_layer(shape, inputs, layer, u_dev, tokens=None):
 
 @pytest.mark.parametrize("name,T", [("tiny_f32", None), ("tiny_f32", 129), ("2b_bf16", 300),
                                     ("16b_bf16", 257), ("16b_decode_bf16", None),
-                                    ("145b_zipf_bf16", 130)])
+                                    ("145b_zipf_bf16", 130), ("2b_half_activated_bf16", 300),
+                                    ("2b_gshard_top2_bf16", 300)])
 def test_layer_all_tokens(name, T):
     shape = C[name]
     inputs = moe_inputs.make_inputs(shape, T=T)
@@ -55,7 +56,8 @@ def test_layer_all_tokens(name, T):
     _compare_layer(shape, inputs, layer, u)
 
 
-@pytest.mark.parametrize("name", ["2b_bf16", "16b_bf16", "145b_zipf_bf16"])
+@pytest.mark.parametrize("name", ["2b_bf16", "16b_bf16", "145b_zipf_bf16",
+                                  "2b_gshard_top2_bf16"])
 def test_layer_full_size_sampled(name):
     """Full token count in the launch configuration the benchmark times; every routing decision
     is compared, h on a seeded sample of tokens (including the first and last tile)."""
@@ -88,6 +90,10 @@ def _custom(**kw):
     dict(n_routed=256, top_k=8, n_groups=8, T=300), # widest router
     dict(dtype="f32", renormalize=1, n_shared=2),
     dict(dtype="f32", top_k=16, n_routed=16, T=77),
+    # ablations of the expert-specialisation analysis: disabled top experts / shared experts
+    dict(skip_top=1), dict(skip_top=3, top_k=2, renormalize=1), dict(skip_top=6, top_k=10),
+    dict(drop_shared=1), dict(drop_shared=1, n_shared=3, skip_top=2),
+    dict(dtype="f32", skip_top=2, drop_shared=1),
 ])
 def test_layer_edge_shapes(kw):
     shape = _custom(**kw)
@@ -167,3 +173,4 @@ def test_graph_replay_matches_direct_calls():
     assert torch.equal(idx_graph, layer.topk_idx)
     assert torch.equal(P_graph, layer.P)
     assert layer.device_status() == 0
+

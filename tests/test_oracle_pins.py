@@ -349,3 +349,64 @@ def test_printed_constants():
         for f, v in g[key].items():
             assert getattr(sh, f) == v
     assert moe_inputs.CONFIGS["145b_zipf_bf16"].d == g["layer_145b"]["d"]
+
+
+# ------------------------------------------------------------------- ablation options ----
+# "DeepSeekMoE 论文解读" §专家特化深度分析: the analysis disables each token's top routed experts
+# (routing falls to the next-ranked ones) and, separately, disables the shared experts.
+
+def test_skip_top_closed_form(oracle_lib):
+    """With s = (1, 2, 3)/6 (router fixture), disabling the top expert routes top-1 to expert 1
+    with gate 1/3 (renormalised: 1); the decision depends on the gaps of ranks 1-2 and 2-3."""
+    g = _golden("router_closed_form.json")
+    e = np.array([[math.log(v), 0.0] for v in g["centroids_ln_of"]], np.float32)
+    u = np.array(g["u"], np.float32)
+    cfg = OracleCfg(T=1, d=2, n_shared=0, n_routed=3, inter=16, top_k=1, skip_top=1)
+    r = oracle.route(cfg, u, e)
+    assert list(r["topk_idx"][0]) == [1]
+    assert abs(r["topk_gate"][0, 0] - 1 / 3) < 1e-7
+    assert abs(r["margin"][0] - 1 / 6) < 1e-7
+    cfg.renormalize = 1
+    assert oracle.route(cfg, u, e)["topk_gate"][0, 0] == pytest.approx(1.0, abs=1e-12)
+    with pytest.raises(ValueError):   # skip_top + K' beyond N'
+        oracle.route(OracleCfg(T=1, d=2, n_shared=0, n_routed=3, inter=16, top_k=2, skip_top=2),
+                     u, e)
+
+
+@pytest.mark.parametrize("N,K,r", [(8, 2, 1), (9, 3, 2), (15, 3, 4), (6, 1, 5)])
+def test_skip_top_is_next_ranked_set(oracle_lib, N, K, r):
+    """The routed set with the r best experts disabled is top-(r+K') minus top-r (brute force over
+    subsets for both), gates are the unchanged affinities, and ties fall to lower indices."""
+    rng = np.random.default_rng(100 + N + K + r)
+    T, d = 10, 16
+    inp = _rand_inputs(rng, T, d, 0, N, 16)
+    base = OracleCfg(T=T, d=d, n_shared=0, n_routed=N, inter=16, top_k=K)
+    skip = OracleCfg(T=T, d=d, n_shared=0, n_routed=N, inter=16, top_k=K, skip_top=r)
+    rs = oracle.route(skip, inp["u"], inp["centroids"], want_scores=True)
+    for t in range(T):
+        s = rs["scores"][t]
+        def best(k):
+            return set(max(itertools.combinations(range(N), k),
+                           key=lambda S: sum(s[i] for i in S))) if k else set()
+        assert set(rs["topk_idx"][t]) == best(r + K) - best(r)
+        np.testing.assert_allclose(rs["topk_gate"][t], s[rs["topk_idx"][t]], rtol=1e-15)
+    # all-equal affinities: ranks follow the index, so the chosen experts are r .. r+K'-1
+    rz = oracle.route(skip, inp["u"], np.zeros((N, d), np.float32))
+    assert np.all(rz["topk_idx"] == np.arange(r, r + K))
+    # the softmax itself does not change
+    rb = oracle.route(base, inp["u"], inp["centroids"], want_scores=True)
+    np.testing.assert_array_equal(rb["psum"], rs["psum"])
+
+
+def test_drop_shared_equals_zeroed_shared_experts(oracle_lib):
+    """Disabling the shared experts gives the layer whose shared W_down is zero."""
+    rng = np.random.default_rng(21)
+    T, d, I, Ks, N = 6, 16, 8, 2, 5
+    inp = _rand_inputs(rng, T, d, Ks, N, I)
+    cfg = OracleCfg(T=T, d=d, n_shared=Ks, n_routed=N, inter=I, top_k=2, drop_shared=1)
+    h_drop = oracle.forward_tokens(cfg, inp, range(T))["h"]
+    zeroed = dict(inp)
+    zeroed["w_down"] = inp["w_down"].copy()
+    zeroed["w_down"][:Ks] = 0
+    cfg0 = OracleCfg(T=T, d=d, n_shared=Ks, n_routed=N, inter=I, top_k=2)
+    np.testing.assert_array_equal(h_drop, oracle.forward_tokens(cfg0, zeroed, range(T))["h"])
