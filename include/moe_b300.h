@@ -155,6 +155,26 @@ int moe_device_status(const void* ws, moe_stream_t stream);
 /* Human-readable name of a moe_status value (static string). */
 const char* moe_status_string(int status);
 
+/* ---- permutation without a caller workspace ---- */
+
+/* moe_permute for callers that cannot provide device scratch memory: code that runs where it may
+ * not allocate (an engine that reserves all device memory up front and forbids later cudaMalloc,
+ * a plugin that is handed only its input and output buffers, a latency-critical loop that cannot
+ * afford the synchronisation cudaMalloc/cudaFree imply). The pages have no counterpart of this
+ * call; it computes exactly what moe_permute computes, with the same arguments except `ws`.
+ *   status: device int32 or NULL; cleared by the call, then set to MOE_ERR_CORRUPT_INPUT under the
+ *           same conditions in which moe_permute sets its workspace status word.
+ * Scratch: a fixed 1 MiB array inside this library, held on every GPU that loads the library until
+ * the process exits. Limit: ceil(T / 128) * N' <= 131072 (for example T <= 65536 at N' = 256,
+ * T <= 262144 at N' = 64); larger configurations return MOE_ERR_UNSUPPORTED without launching.
+ * The first call on a device looks up the array's device address with that device current; make
+ * that first call before any stream capture. All calls share the array: calls whose kernels can
+ * overlap on a GPU (different streams, or several host threads) race and must be serialised by
+ * the caller. No device memory is allocated or freed by this call. */
+int moe_permute_static(const moe_config* cfg, const int32_t* topk_idx, const int32_t* counts,
+                       int32_t* offsets, int32_t* perm_token, int32_t* perm_slot,
+                       int32_t* status, moe_stream_t stream);
+
 /* ---- failure detection ---- */
 
 /* Self-test of the bounded waits that every pipelined kernel of this library uses: launches one
