@@ -319,3 +319,151 @@ int oracle_threads(void) {
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------ backward ---- */
+
+/* Gradients of the training objective
+ *     Lambda = sum_t dh_t . h_t + L_ExpBal + L_DevBal
+ * with respect to the layer inputs and parameters, for the given upstream gradient dh [T, d].
+ * The expert selection and the counts (hence f_j and f'_g) are piecewise constant and are held
+ * fixed, as the pages' losses use them ([P1] §方法细节: f_i is a selection frequency, P_i the
+ * mean affinity; [P2] §2.3, §2.4). Per token t, with chosen experts c_k (ranks skip..skip+K'-1):
+ *   h_t = u_t + sum_shared FFN_s(u_t) + sum_k g_k FFN_{c_k}(u_t)
+ *   dFFN input/weights by the chain rule through y = W_d (silu(a) * b), a = W_g x, b = W_u x,
+ *     silu'(a) = sig(a) (1 + a (1 - sig(a)));
+ *   dgate_k = dh_t . FFN_{c_k}(u_t);  ds_j = dgate (through g = s or s / sum_chosen s)
+ *            + a1 f_j / T + a2 f'_{group(j)} / T;
+ *   dz_j = s_j (ds_j - sum_m s_m ds_m);  du_t += sum_j dz_j e_j;  de_j += dz_j u_t;  db_j += dz_j.
+ * Outputs (all fp64, overwritten): du [T, d], d_cent [N', d], d_bias [N'], dw_gate / dw_up
+ * [E, I, d], dw_down [E, d, I]. counts [N'] are the selection counts of this batch (as routed by
+ * the oracle when NULL). Tokens run in order, one at a time. */
+int oracle_backward(const oracle_cfg* c, const void* u, const void* centroids, const float* bias,
+                    const void* w_gate, const void* w_up, const void* w_down, const double* dh,
+                    const int64_t* counts_in, double* du, double* d_cent, double* d_bias,
+                    double* dw_gate, double* dw_up, double* dw_down) {
+    const int T = c->T, d = c->d, N = c->n_routed, K = c->top_k, I = c->inter, Ks = c->n_shared;
+    const int E = Ks + N;
+    if (T < 1 || c->skip_top < 0 || c->skip_top + K > N || c->n_groups < 1 || c->n_groups > N)
+        return -1;
+    int64_t* counts = (int64_t*)calloc((size_t)N, sizeof(int64_t));
+    double* s = (double*)malloc(sizeof(double) * (size_t)N);
+    int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)K);
+    double* g = (double*)malloc(sizeof(double) * (size_t)K);
+    double m;
+    if (counts_in) {
+        for (int j = 0; j < N; ++j) counts[j] = counts_in[j];
+    } else {
+        for (int t = 0; t < T; ++t) {
+            oracle_token_route(c, u, centroids, bias, t, s, idx, g, &m);
+            for (int k = 0; k < K; ++k) counts[idx[k]] += 1;
+        }
+    }
+    /* f_j and the group means f'_g (constants of the backward) */
+    double* fj = (double*)malloc(sizeof(double) * (size_t)N);
+    double* fgrp = (double*)malloc(sizeof(double) * (size_t)N);   /* f' of expert j's group */
+    for (int j = 0; j < N; ++j) fj[j] = (double)N / ((double)K * (double)T) * (double)counts[j];
+    for (int gi = 0; gi < c->n_groups; ++gi) {
+        int first, size;
+        oracle_group_range(N, c->n_groups, gi, &first, &size);
+        double mean = 0.0;
+        for (int j = first; j < first + size; ++j) mean += fj[j];
+        mean /= (double)size;
+        for (int j = first; j < first + size; ++j) fgrp[j] = mean;
+    }
+    memset(du, 0, sizeof(double) * (size_t)T * d);
+    memset(d_cent, 0, sizeof(double) * (size_t)N * d);
+    memset(d_bias, 0, sizeof(double) * (size_t)N);
+    memset(dw_gate, 0, sizeof(double) * (size_t)E * I * d);
+    memset(dw_up, 0, sizeof(double) * (size_t)E * I * d);
+    memset(dw_down, 0, sizeof(double) * (size_t)E * d * I);
+
+    double* x = (double*)malloc(sizeof(double) * (size_t)d);
+    double* a = (double*)malloc(sizeof(double) * (size_t)I);
+    double* b = (double*)malloc(sizeof(double) * (size_t)I);
+    double* act = (double*)malloc(sizeof(double) * (size_t)I);
+    double* y = (double*)malloc(sizeof(double) * (size_t)d);
+    double* dy = (double*)malloc(sizeof(double) * (size_t)d);
+    double* dact = (double*)malloc(sizeof(double) * (size_t)I);
+    double* ds = (double*)malloc(sizeof(double) * (size_t)N);
+    double* dgate = (double*)malloc(sizeof(double) * (size_t)K);
+
+    for (int t = 0; t < T; ++t) {
+        for (int k = 0; k < d; ++k) x[k] = elem(u, c->dtype, (size_t)t * d + k);
+        oracle_token_route(c, u, centroids, bias, t, s, idx, g, &m);
+        const double* dht = dh + (size_t)t * d;
+        double* dut = du + (size_t)t * d;
+        for (int k = 0; k < d; ++k) dut[k] = dht[k];                 /* residual */
+        /* experts: shared (gate 1, unless disabled) then the chosen routed ones */
+        const int n_sh = c->drop_shared ? 0 : Ks;
+        for (int q = 0; q < n_sh + K; ++q) {
+            const int e = q < n_sh ? q : Ks + idx[q - n_sh];
+            const double gate = q < n_sh ? 1.0 : g[q - n_sh];
+            const size_t gu0 = (size_t)e * I * d, dn0 = (size_t)e * d * I;
+            for (int i = 0; i < I; ++i) {
+                double av = 0.0, bv = 0.0;
+                for (int k = 0; k < d; ++k) {
+                    av += elem(w_gate, c->dtype, gu0 + (size_t)i * d + k) * x[k];
+                    bv += elem(w_up, c->dtype, gu0 + (size_t)i * d + k) * x[k];
+                }
+                a[i] = av;
+                b[i] = bv;
+                act[i] = av / (1.0 + exp(-av)) * bv;
+            }
+            if (q >= n_sh) {   /* dgate = dh . y */
+                double dot = 0.0;
+                for (int n = 0; n < d; ++n) {
+                    double acc = 0.0;
+                    for (int i = 0; i < I; ++i)
+                        acc += elem(w_down, c->dtype, dn0 + (size_t)n * I + i) * act[i];
+                    dot += dht[n] * acc;
+                }
+                dgate[q - n_sh] = dot;
+            }
+            for (int n = 0; n < d; ++n) dy[n] = gate * dht[n];
+            for (int i = 0; i < I; ++i) {
+                double acc = 0.0;
+                for (int n = 0; n < d; ++n)
+                    acc += elem(w_down, c->dtype, dn0 + (size_t)n * I + i) * dy[n];
+                dact[i] = acc;
+            }
+            for (int n = 0; n < d; ++n)
+                for (int i = 0; i < I; ++i) dw_down[dn0 + (size_t)n * I + i] += dy[n] * act[i];
+            for (int i = 0; i < I; ++i) {
+                const double sg = 1.0 / (1.0 + exp(-a[i]));
+                const double silu = a[i] * sg;
+                const double da = dact[i] * b[i] * sg * (1.0 + a[i] * (1.0 - sg));
+                const double db = dact[i] * silu;
+                for (int k = 0; k < d; ++k) {
+                    dw_gate[gu0 + (size_t)i * d + k] += da * x[k];
+                    dw_up[gu0 + (size_t)i * d + k] += db * x[k];
+                    dut[k] += da * elem(w_gate, c->dtype, gu0 + (size_t)i * d + k) +
+                              db * elem(w_up, c->dtype, gu0 + (size_t)i * d + k);
+                }
+            }
+        }
+        /* router: gates -> affinities (+ balance-loss terms) -> logits */
+        for (int j = 0; j < N; ++j)
+            ds[j] = (c->alpha1 * fj[j] + c->alpha2 * fgrp[j]) / (double)T;
+        if (c->renormalize) {
+            double S = 0.0, w = 0.0;
+            for (int k = 0; k < K; ++k) S += s[idx[k]];
+            for (int k = 0; k < K; ++k) w += dgate[k] * s[idx[k]];
+            for (int k = 0; k < K; ++k) ds[idx[k]] += dgate[k] / S - w / (S * S);
+        } else {
+            for (int k = 0; k < K; ++k) ds[idx[k]] += dgate[k];
+        }
+        double sds = 0.0;
+        for (int j = 0; j < N; ++j) sds += s[j] * ds[j];
+        for (int j = 0; j < N; ++j) {
+            const double dz = s[j] * (ds[j] - sds);
+            d_bias[j] += dz;
+            for (int k = 0; k < d; ++k) {
+                dut[k] += dz * elem(centroids, c->dtype, (size_t)j * d + k);
+                d_cent[(size_t)j * d + k] += dz * x[k];
+            }
+        }
+    }
+    free(counts); free(s); free(idx); free(g); free(fj); free(fgrp); free(x); free(a); free(b);
+    free(act); free(y); free(dy); free(dact); free(ds); free(dgate);
+    return 0;
+}

@@ -92,6 +92,7 @@ def _load():
         lib.oracle_group_range.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
         lib.oracle_group_range.restype = None
         lib.oracle_threads.restype = ctypes.c_int
+        lib.oracle_backward.argtypes = [cfgp, P, P, P, P, P, P, P, P, P, P, P, P, P, P]
         _lib = lib
     return _lib
 
@@ -251,4 +252,28 @@ def layer_forward(cfg: OracleCfg, inputs: dict, tokens: Optional[Sequence[int]] 
     out.update(st)
     out["tokens"] = toks
     out["h"] = fw["h"]
+    return out
+
+
+def backward(cfg: OracleCfg, inputs: dict, dh, counts=None) -> dict:
+    """Gradients of sum_t dh_t . h_t + L_ExpBal + L_DevBal (selection and counts held fixed)."""
+    lib = _load()
+    T, d, N, I = cfg.T, cfg.d, cfg.n_routed, cfg.inter
+    E = cfg.n_shared + N
+    u_ = _raw(inputs["u"], cfg.dtype)
+    e_ = _raw(inputs["centroids"], cfg.dtype)
+    b_ = _bias(inputs.get("bias"))
+    wg, wu, wd = (_raw(inputs[k], cfg.dtype) for k in ("w_gate", "w_up", "w_down"))
+    dh_ = np.ascontiguousarray(np.asarray(dh, dtype=np.float64).reshape(T, d))
+    cnt = None if counts is None else np.ascontiguousarray(np.asarray(counts), dtype=np.int64)
+    out = {"du": np.zeros((T, d)), "d_centroids": np.zeros((N, d)), "d_bias": np.zeros(N),
+           "dw_gate": np.zeros((E, I, d)), "dw_up": np.zeros((E, I, d)),
+           "dw_down": np.zeros((E, d, I))}
+    c = cfg.c()
+    rc = lib.oracle_backward(ctypes.byref(c), _p(u_), _p(e_), _p(b_), _p(wg), _p(wu), _p(wd),
+                             _p(dh_), _p(cnt), _p(out["du"]), _p(out["d_centroids"]),
+                             _p(out["d_bias"]), _p(out["dw_gate"]), _p(out["dw_up"]),
+                             _p(out["dw_down"]))
+    if rc != 0:
+        raise ValueError("oracle_backward rejected its arguments")
     return out
