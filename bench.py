@@ -268,32 +268,52 @@ def run_ours(args, sh, rank, world, local_rank):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
 
-    # ---- end to end through host buffers: H2D of u, the layer, D2H of h and the losses ----
-    h_host = torch.empty(T, sh.d, dtype=u.dtype).pin_memory()
-    loss_host = torch.empty(2, dtype=torch.float32).pin_memory()
-    u_dev = torch.empty_like(u)
+    # ---- end to end through host buffers. Every step copies its T tokens in from pinned host
+    # memory, runs the layer call and copies h and the two losses out to pinned host memory. The
+    # copies run on their own streams with double-buffered device buffers, so step i's input copy
+    # and step i-1's output copy overlap the layer calls; the timed region spans the first input
+    # copy to the last output copy. ----
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    u_devs = [torch.empty_like(u) for _ in range(2)]
+    h_devs = [torch.empty(T, sh.d, dtype=u.dtype, device=dev) for _ in range(2)]
+    loss_devs = [torch.empty(2, dtype=torch.float32, device=dev) for _ in range(2)]
+    h_hosts = [torch.empty(T, sh.d, dtype=u.dtype).pin_memory() for _ in range(2)]
+    loss_hosts = [torch.empty(2, dtype=torch.float32).pin_memory() for _ in range(2)]
 
-    def e2e_step():
-        u_dev.copy_(u_host, non_blocking=True)
-        layer.forward(u_dev)
-        h_host.copy_(layer.h, non_blocking=True)
-        loss_host.copy_(layer.losses, non_blocking=True)
+    def e2e_run(n_steps):
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        copied = [torch.cuda.Event() for _ in range(2)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        t0.record(h2d)
+        for i in range(n_steps):
+            b = i % 2
+            if i >= 2:
+                h2d.wait_event(done[b])        # step i-2 has finished reading u_devs[b]
+            with torch.cuda.stream(h2d):
+                u_devs[b].copy_(u_host, non_blocking=True)
+                in_ready[b].record(h2d)
+            stream.wait_event(in_ready[b])
+            if i >= 2:
+                stream.wait_event(copied[b])   # step i-2's outputs have left h_devs[b]
+            layer.forward(u_devs[b], h=h_devs[b], stream=stream)
+            loss_devs[b].copy_(layer.losses)
+            done[b].record(stream)
+            d2h.wait_event(done[b])
+            with torch.cuda.stream(d2h):
+                h_hosts[b].copy_(h_devs[b], non_blocking=True)
+                loss_hosts[b].copy_(loss_devs[b], non_blocking=True)
+                copied[b].record(d2h)
+        t1.record(d2h)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1)
 
-    for _ in range(max(args.warmup, 3)):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e2e_run(max(args.warmup, 3))
     barrier()
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        e_starts[i].record(stream)
-        e2e_step()
-        e_ends[i].record(stream)
-    torch.cuda.synchronize(dev)
+    e2e_ms = e2e_run(args.steps)
     barrier()
     clk = clocks.stop()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends))
     status = layer.device_status()
     if status != 0:
         raise RuntimeError(f"device status {moe.moe_status_string(status)} after timing")
@@ -330,7 +350,9 @@ def run_ours(args, sh, rank, world, local_rank):
                            layer_tflops / bf16_tf, "flops_per_token": flops_per_token(sh)},
         "stage_ms_per_step": {k: v / max(n_prof, 1) for k, v in stage_ms.items()},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * sh.d * u.element_size(),
-                "d2h_bytes_per_step": T * sh.d * u.element_size() + 8},
+                "d2h_bytes_per_step": T * sh.d * u.element_size() + 8,
+                "copies": "pinned host buffers; input and output copies on their own streams, "
+                          "overlapping the neighbouring steps' layer calls"},
         "gpu_launches": launches,
         "clocks": clk,
     }
@@ -343,6 +365,67 @@ def run_ours(args, sh, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def backward_flops_per_token(sh) -> float:
+    """GEMM FLOPs one moe_layer_backward call executes per token: the forward it recomputes
+    (router 2 d N', gate/up 4 d I (Ks+K'), routed down 2 d I K') and the gradients (router 2 x
+    2 d N', input gradients 6 d I (Ks+K'), weight gradients 6 d I (Ks+K'))."""
+    A = sh.n_shared + sh.top_k
+    return (2.0 * sh.d * sh.n_routed * 3 + 4.0 * sh.d * sh.inter * A + 2.0 * sh.d * sh.inter *
+            sh.top_k + 12.0 * sh.d * sh.inter * A)
+
+
+def run_backward(args, sh):
+    """Times moe_layer_backward (gradients of sum dh.h + the balance losses); one JSON line."""
+    import torch
+
+    import fine_grained_moe_softmax_b300 as moe
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inputs = moe_inputs.make_inputs(sh)
+    layer = moe.MoELayer(moe.MoEConfig.from_shape(sh), inputs["centroids"], inputs["w_gate"],
+                         inputs["w_up"], inputs["w_down"], inputs["bias"], device=dev,
+                         backward=True)
+    u = inputs["u"].to(dev)
+    g = torch.Generator().manual_seed(sh.seed + 5)
+    dh = torch.randn(sh.T, sh.d, generator=g).to(torch.bfloat16).to(dev)
+    del inputs
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        layer.backward(u, dh)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    n0 = moe.moe_launch_count()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        layer.backward(u, dh)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = moe.moe_launch_count() - n0
+    clk = clocks.stop()
+    if moe.moe_device_status(layer.ws_bwd) != 0:
+        raise RuntimeError("device status after the backward")
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    _, bf16_tf, _, peak_src = load_peaks()
+    tflops = backward_flops_per_token(sh) * sh.T / (total_ms / args.steps / 1e3) / 1e12
+    print(json.dumps({
+        "metric": "MoE-layer backward tokens/s (gradients of u, centroids, bias, all experts)",
+        "value": sh.T * args.steps / (total_ms / 1e3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "dtype": sh.dtype, "data": "synthetic",
+        "config": {"workload": sh.name, "T": sh.T, "d": sh.d, "n_shared": sh.n_shared,
+                   "n_routed": sh.n_routed, "inter": sh.inter, "top_k": sh.top_k,
+                   "note": "one call recomputes the forward it needs"},
+        "executed_tflops": tflops, "frac_of_bf16_peak": tflops / bf16_tf,
+        "peak_source": f"{peak_src} bf16 burst", "gpu_launches": launches, "clocks": clk}),
+        flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -353,6 +436,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=512)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the layer backward instead of the forward (1 GPU)")
     ap.add_argument("--graph", action="store_true",
                     help="time CUDA-graph replays of the layer call instead of direct calls")
     ap.add_argument("--tokens", type=int, default=None,
@@ -376,7 +461,9 @@ def main():
             torch.cuda.set_device(local_rank)
         dist.init_process_group(backend)
     try:
-        if args.impl == "reference":
+        if args.backward:
+            run_backward(args, sh)
+        elif args.impl == "reference":
             run_reference(args, sh, rank, world)
         else:
             run_ours(args, sh, rank, world, local_rank)

@@ -61,6 +61,11 @@ _SIG = {
     "moe_balance_stats": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_layer_forward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.c_size_t, _P]),
+    "moe_backward_workspace_bytes": (ctypes.c_size_t, [_CFG]),
+    "moe_packed_backward_bytes": (ctypes.c_size_t, [_CFG]),
+    "moe_pack_weights_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_layer_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          _P, ctypes.c_size_t, _P]),
     "moe_device_status": (ctypes.c_int, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_selftest_bounded_wait": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint64, _P]),
@@ -172,6 +177,29 @@ def moe_layer_forward(cfg, u, centroids, logit_bias, packed_w, h, topk_idx, topk
                                    _ptr(packed_w), _ptr(h), _ptr(topk_idx), _ptr(topk_gate),
                                    _ptr(counts), _ptr(f), _ptr(P), _ptr(losses), _ptr(ws),
                                    _nbytes(ws), _stream(stream)), "moe_layer_forward")
+
+
+def moe_backward_workspace_bytes(cfg: MoEConfig) -> int:
+    return int(lib().moe_backward_workspace_bytes(ctypes.byref(cfg)))
+
+
+def moe_packed_backward_bytes(cfg: MoEConfig) -> int:
+    return int(lib().moe_packed_backward_bytes(ctypes.byref(cfg)))
+
+
+def moe_pack_weights_backward(cfg, w_gate, w_up, w_down, packed_bwd, stream=None):
+    _check(lib().moe_pack_weights_backward(ctypes.byref(cfg), _ptr(w_gate), _ptr(w_up),
+                                           _ptr(w_down), _ptr(packed_bwd), _stream(stream)),
+           "moe_pack_weights_backward")
+
+
+def moe_layer_backward(cfg, u, centroids, logit_bias, packed_w, packed_bwd, dh, du, d_centroids,
+                       d_bias, dw_gate, dw_up, dw_down, ws, stream=None):
+    _check(lib().moe_layer_backward(ctypes.byref(cfg), _ptr(u), _ptr(centroids), _ptr(logit_bias),
+                                    _ptr(packed_w), _ptr(packed_bwd), _ptr(dh), _ptr(du),
+                                    _ptr(d_centroids), _ptr(d_bias), _ptr(dw_gate), _ptr(dw_up),
+                                    _ptr(dw_down), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "moe_layer_backward")
 
 
 def moe_device_status(ws, stream=None) -> int:

@@ -97,6 +97,79 @@ inline PackLayout pack_layout(const Dims& m) {
     return P;
 }
 
+// Transposed expert weights for the input gradients of the backward (element offsets):
+//   W_down^T per routed expert [N, I, d], shared [Ks*I, d];
+//   packed gate/up^T per routed expert [N, d, 2I], shared [d, 2*Ks*I] (packed column order).
+struct PackBwdLayout {
+    size_t wdT_r, wdT_s, wguT_r, wguT_s, total;
+};
+
+inline PackBwdLayout pack_bwd_layout(const Dims& m) {
+    PackBwdLayout P{};
+    const size_t Id = (size_t)m.I * m.d;
+    P.wdT_r = 0;
+    P.wdT_s = P.wdT_r + (size_t)m.N * Id;
+    P.wguT_r = P.wdT_s + (size_t)m.Ks * Id;
+    P.wguT_s = P.wguT_r + (size_t)m.N * 2 * Id;
+    P.total = P.wguT_s + (size_t)m.Ks * 2 * Id;
+    return P;
+}
+
+// Rows of the padded per-expert segments used by the backward: every expert's segment starts at
+// a multiple of 64, so at most 63 padding rows per expert follow its T*K' real rows.
+inline size_t padded_rows(const Dims& m) { return (size_t)m.T * m.K + (size_t)63 * m.N; }
+
+// Byte offsets of the backward's scratch inside the caller's workspace (256-byte aligned).
+struct BwdLayout {
+    size_t status, tile_counts, tile_psum, tile_base, tile_dz;
+    size_t psum, poff, counts, topk_idx, gate, perm_token, perm_slot, dgate;
+    size_t x_perm, pre_r, act_r, y_r, d_y, d_gu_r, d_x_r;   // [R, .] routed rows
+    size_t pre_s, act_s, d_gu_s, d_x_s;                        // [T, .] shared
+    size_t dz, eT, d_u_r;
+    size_t total;
+    int n_tiles;
+    size_t R;
+};
+
+inline BwdLayout bwd_layout(const Dims& m) {
+    BwdLayout L{};
+    const size_t T = m.T, K = m.K, N = m.N, d = m.d, I = m.I, KsI = (size_t)m.Ks * m.I;
+    const size_t R = padded_rows(m), npad = (m.N + 31) / 32 * 32;
+    L.n_tiles = (m.T + kRouteTile - 1) / kRouteTile;
+    L.R = R;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+    L.status = take(256);
+    L.tile_counts = take((size_t)L.n_tiles * N * 4);
+    L.tile_psum = take((size_t)L.n_tiles * N * 4);
+    L.tile_base = take((size_t)L.n_tiles * N * 4);
+    L.tile_dz = take((size_t)L.n_tiles * N * 4);
+    L.psum = take(N * 4);
+    L.poff = take((N + 1) * 4);
+    L.counts = take(N * 4);
+    L.topk_idx = take(T * K * 4);
+    L.gate = take(T * K * 4);
+    L.perm_token = take(R * 4);
+    L.perm_slot = take(T * K * 4);
+    L.dgate = take(T * K * 4);
+    L.x_perm = take(R * d * 2);
+    L.pre_r = take(R * 2 * I * 2);
+    L.act_r = take(R * I * 2);
+    L.y_r = take(R * d * 2);
+    L.d_y = take(R * d * 2);
+    L.d_gu_r = take(R * 2 * I * 2);
+    L.d_x_r = take(R * d * 2);
+    L.pre_s = take(T * 2 * KsI * 2);
+    L.act_s = take(T * KsI * 2);
+    L.d_gu_s = take(T * 2 * KsI * 2);
+    L.d_x_s = take(T * d * 2);
+    L.dz = take(T * npad * 2);
+    L.eT = take(d * npad * 2);
+    L.d_u_r = take(T * d * 2);
+    L.total = o;
+    return L;
+}
+
 // ------------------------------------------------------------------------ device utils ----
 
 // First error wins; later errors leave the word alone.

@@ -73,6 +73,7 @@ constexpr int kThreads = 192;
 struct TcArgs {
     CUtensorMap a_r, a_s, b_r, b_s;
     const int* offsets;
+    const int* counts;            // optional: rows per routed group (padded segments)
     GroupTiles gt;
     int k_blocks_r, k_blocks_s;
     int b_rows_per_expert;
@@ -80,6 +81,9 @@ struct TcArgs {
     __nv_bfloat16* out_r;
     __nv_bfloat16* out_s;
     int ld_r, ld_s;
+    __nv_bfloat16* pre_r;         // optional (gate/up): raw accumulator values, packed columns
+    __nv_bfloat16* pre_s;
+    int ld_pre_r, ld_pre_s;
     int* status;
 };
 
@@ -98,7 +102,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int BN, int STAGES, bool GATEUP>
+// EPI: 0 plain bf16 store; 1 SwiGLU of packed gate/up column pairs (expert FFN forward);
+// 2 SwiGLU backward: the accumulator is d_act, and with the saved gate/up values of the same rows
+// (pre, packed) the epilogue writes d_gate / d_up (packed) to out.
+template <int BN, int STAGES, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcArgs args) {
     using S = Smem<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
@@ -146,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     }
     pdl_wait();
     pdl_trigger();
-    build_tile_prefix<BM>(prefix, rows_s, row0_s, args.offsets, gt);   // contains __syncthreads
+    build_tile_prefix<BM>(prefix, rows_s, row0_s, args.offsets, gt, args.counts);   // syncs
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -274,7 +281,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 ptx::tmem_ld_32x32b_x32(t_base + c * 32, v);
                 ptx::tmem_ld_wait();
                 if (!valid) continue;
-                if constexpr (GATEUP) {
+                if constexpr (EPI == 1) {
+                    __nv_bfloat16* pre = sh ? args.pre_s : args.pre_r;
+                    if (pre) {   // the raw gate/up values, kept for the backward
+                        uint32_t p[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            p[q] = pack_bf16x2(__uint_as_float(v[2 * q]),
+                                               __uint_as_float(v[2 * q + 1]));
+                        uint4* pd = reinterpret_cast<uint4*>(
+                            pre + (size_t)(ti.row0 + r) * (sh ? args.ld_pre_s : args.ld_pre_r) + col0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            pd[q] = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+                    }
                     uint32_t o[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -286,15 +306,52 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     uint4* dst = reinterpret_cast<uint4*>(out + orow + col0 / 2);
                     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
                     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                } else if constexpr (EPI == 2) {
+                    // columns col0 .. col0+31 are intermediate indices i; their gate/up values
+                    // sit in packed blocks col0/16 and col0/16 + 1 (32 values each)
+                    const __nv_bfloat16* pre = sh ? args.pre_s : args.pre_r;
+                    const size_t prow = (size_t)(ti.row0 + r) * (sh ? args.ld_pre_s : args.ld_pre_r);
+                    const int halves = col0 + 16 < n_cols ? 2 : 1;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (h < halves) {
+                            const uint4* src = reinterpret_cast<const uint4*>(pre + prow + 2 * col0 +
+                                                                              32 * h);
+                            uint4 raw[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) raw[q] = src[q];
+                            const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(raw);
+                            uint32_t o[16];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float2 g2 = __bfloat1622float2(p2[q]);       // gate
+                                const float2 u2 = __bfloat1622float2(p2[8 + q]);   // up
+                                const float da0 = __uint_as_float(v[16 * h + 2 * q]);
+                                const float da1 = __uint_as_float(v[16 * h + 2 * q + 1]);
+                                const float s0 = 1.0f / (1.0f + __expf(-g2.x));
+                                const float s1 = 1.0f / (1.0f + __expf(-g2.y));
+                                o[q] = pack_bf16x2(da0 * u2.x * s0 * (1.0f + g2.x * (1.0f - s0)),
+                                                   da1 * u2.y * s1 * (1.0f + g2.y * (1.0f - s1)));
+                                o[8 + q] = pack_bf16x2(da0 * g2.x * s0, da1 * g2.y * s1);
+                            }
+                            uint4* dst = reinterpret_cast<uint4*>(out + orow + 2 * col0 + 32 * h);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        }
+                    }
                 } else {
                     uint32_t o[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q)
                         o[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
                     uint4* dst = reinterpret_cast<uint4*>(out + orow + col0);
+                    // widths are multiples of 16: the second half of a chunk may lie past the end
+                    const int halves = col0 + 16 < n_cols ? 2 : 1;
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        if (q < 2 * halves)
+                            dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                 }
             }
             ptx::tc_fence_before();
@@ -317,10 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
 // ------------------------------------------------------------------------- host side ----
 
-template <int BN, int STAGES, bool GATEUP>
+template <int BN, int STAGES, int EPI>
 cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
     using S = Smem<BN, STAGES>;
-    auto kern = gemm_tc_kernel<BN, STAGES, GATEUP>;
+    auto kern = gemm_tc_kernel<BN, STAGES, EPI>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), S::total);
     if (e != cudaSuccess) return e;
     const int grid = max(1, min(sm_count(), max_tiles));
@@ -330,36 +387,46 @@ cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-struct GemmShape {
-    const void *a_r, *a_s, *b_r, *b_s;
-    uint64_t a_rows_r, a_rows_s, k_r, k_s;     // A rows and K extents
-    uint64_t b_rows_r, b_rows_s;              // B total rows
-    int b_rows_per_expert, n_cols_r, n_cols_s;
-    void *out_r, *out_s;
-    int ld_r, ld_s;
-};
+// 256-column tiles unless they would waste more than a tenth of the computed columns.
+int pick_bn(int n_r, int n_s) {
+    long pad256 = 0, pad128 = 0, cols = 0;
+    for (int n : {n_r, n_s}) {
+        if (n <= 0) continue;
+        cols += n;
+        pad256 += (n + 255) / 256 * 256;
+        pad128 += (n + 127) / 128 * 128;
+    }
+    if (cols == 0) return 256;
+    return (pad256 - cols) * 10 <= pad256 || pad256 <= pad128 ? 256 : 128;
+}
 
-template <bool GATEUP>
-cudaError_t run_gemm(const Dims& m, const GemmShape& g, const int* offsets, int* status,
-                     cudaStream_t st) {
-    const bool shared = m.shared_active();
-    const int bn = (g.n_cols_r % 256 == 0 && (!shared || g.n_cols_s % 256 == 0)) ? 256 : 128;
+template <int EPI>
+cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
+    const bool shared = g.has_shared;
+    const int bn = pick_bn(g.n_routed > 0 ? g.n_cols_r : 0, shared ? g.n_cols_s : 0);
     TcArgs a{};
-    if (!encode_bf16_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, BM) ||
-        !encode_bf16_map(&a.b_r, g.b_r, g.b_rows_r, g.k_r, bn))
-        return cudaErrorInvalidValue;
+    if (g.n_routed > 0) {
+        if (!encode_bf16_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, BM) ||
+            !encode_bf16_map(&a.b_r, g.b_r, g.b_rows_r, g.k_r, bn))
+            return cudaErrorInvalidValue;
+    }
     if (shared) {
         if (!encode_bf16_map(&a.a_s, g.a_s, g.a_rows_s, g.k_s, BM) ||
             !encode_bf16_map(&a.b_s, g.b_s, g.b_rows_s, g.k_s, bn))
             return cudaErrorInvalidValue;
-    } else {
-        a.a_s = a.a_r;   // the shared group is empty and never loads
+    }
+    if (g.n_routed == 0) {   // a dense GEMM: only the shared slot has rows
+        a.a_r = a.a_s;
+        a.b_r = a.b_s;
+    } else if (!shared) {    // the shared group is empty and never loads
+        a.a_s = a.a_r;
         a.b_s = a.b_r;
     }
-    a.offsets = offsets;
-    a.gt.n_groups = 1 + m.N;
+    a.offsets = g.offsets;
+    a.counts = g.counts;
+    a.gt.n_groups = 1 + g.n_routed;
     a.gt.has_shared = shared;
-    a.gt.T = m.T;
+    a.gt.T = g.T_shared;
     a.gt.n_tiles_r = (g.n_cols_r + bn - 1) / bn;
     a.gt.n_tiles_s = shared ? (g.n_cols_s + bn - 1) / bn : 0;
     a.k_blocks_r = (int)((g.k_r + BK - 1) / BK);
@@ -371,13 +438,18 @@ cudaError_t run_gemm(const Dims& m, const GemmShape& g, const int* offsets, int*
     a.out_s = static_cast<__nv_bfloat16*>(g.out_s);
     a.ld_r = g.ld_r;
     a.ld_s = g.ld_s;
+    a.pre_r = static_cast<__nv_bfloat16*>(g.pre_r);
+    a.pre_s = static_cast<__nv_bfloat16*>(g.pre_s);
+    a.ld_pre_r = g.ld_pre_r;
+    a.ld_pre_s = g.ld_pre_s;
     a.status = status;
-    // upper bound of the tiles: sum over experts of ceil(M_j / 128) <= T*K'/128 + N'
-    const long routed_mblk = (long)m.T * m.K / BM + m.N;
-    const long max_tiles = routed_mblk * a.gt.n_tiles_r + (long)((m.T + BM - 1) / BM) * a.gt.n_tiles_s;
+    // upper bound of the tiles: sum over groups of ceil(M_j / 128) <= rows/128 + groups
+    const long routed_mblk = g.n_routed > 0 ? (long)(g.max_routed_rows / BM) + g.n_routed : 0;
+    const long max_tiles = routed_mblk * a.gt.n_tiles_r +
+                           (long)((g.T_shared + BM - 1) / BM) * a.gt.n_tiles_s;
     const int mt = (int)std::min<long>(max_tiles, 1 << 30);
-    if (bn == 256) return launch_tc<256, 4, GATEUP>(a, mt, st);
-    return launch_tc<128, 6, GATEUP>(a, mt, st);
+    if (bn == 256) return launch_tc<256, 4, EPI>(a, mt, st);
+    return launch_tc<128, 6, EPI>(a, mt, st);
 }
 
 }  // namespace
@@ -396,7 +468,12 @@ cudaError_t launch_expert_gemms(const Dims& m, const void* u, const void* x_perm
     const PackLayout P = pack_layout(m);
     const char* pk = static_cast<const char*>(packed);
     const uint64_t TK = (uint64_t)m.T * m.K, KsI = (uint64_t)m.Ks * m.I;
-    GemmShape gu{};
+    GroupedGemm gu{};
+    gu.n_routed = m.N;
+    gu.has_shared = m.shared_active();
+    gu.T_shared = m.T;
+    gu.offsets = offsets;
+    gu.max_routed_rows = (long)TK;
     gu.a_r = x_perm;
     gu.a_s = u;
     gu.b_r = pk + P.gu_r * 2;
@@ -413,16 +490,14 @@ cudaError_t launch_expert_gemms(const Dims& m, const void* u, const void* x_perm
     gu.out_s = act_s;
     gu.ld_r = m.I;
     gu.ld_s = (int)KsI;
-    cudaError_t e = run_gemm<true>(m, gu, offsets, status, st);
+    cudaError_t e = run_gemm<1>(gu, status, st);
     if (e != cudaSuccess) return e;
     if (mid_event) cudaEventRecord(mid_event, st);
-    GemmShape dn{};
+    GroupedGemm dn = gu;
     dn.a_r = act_r;
     dn.a_s = act_s;
     dn.b_r = pk + P.dn_r * 2;
     dn.b_s = pk + P.dn_s * 2;
-    dn.a_rows_r = TK;
-    dn.a_rows_s = m.T;
     dn.k_r = m.I;
     dn.k_s = KsI;
     dn.b_rows_r = (uint64_t)m.N * m.d;
@@ -432,7 +507,13 @@ cudaError_t launch_expert_gemms(const Dims& m, const void* u, const void* x_perm
     dn.out_r = y_r;
     dn.out_s = y_s;
     dn.ld_r = dn.ld_s = m.d;
-    return run_gemm<false>(m, dn, offsets, status, st);
+    return run_gemm<0>(dn, status, st);
+}
+
+cudaError_t run_grouped_gemm(const GroupedGemm& g, int epilogue, int* status, cudaStream_t st) {
+    if (epilogue == 1) return run_gemm<1>(g, status, st);
+    if (epilogue == 2) return run_gemm<2>(g, status, st);
+    return run_gemm<0>(g, status, st);
 }
 
 }  // namespace moe

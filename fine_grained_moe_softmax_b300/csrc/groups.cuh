@@ -27,18 +27,21 @@ struct TileInfo {
 };
 
 // Fills prefix[0 .. n_groups] (shared memory) from offsets; every thread of the CTA must call it.
+// With `counts`, routed expert j has counts[j] rows starting at offsets[j] (padded segments);
+// otherwise its rows are offsets[j] .. offsets[j+1]-1.
 template <int BM>
 __device__ __forceinline__ void build_tile_prefix(int* prefix, int* rows_s, int* row0_s,
                                                   const int* __restrict__ offsets,
-                                                  const GroupTiles& gt) {
+                                                  const GroupTiles& gt,
+                                                  const int* __restrict__ counts = nullptr) {
     const int N = gt.n_groups - 1;
     for (int j = threadIdx.x; j <= N; j += blockDim.x) {
         if (j == 0) {
             rows_s[0] = gt.has_shared ? gt.T : 0;
             row0_s[0] = 0;
         } else {
-            const int lo = offsets[j - 1], hi = offsets[j];
-            rows_s[j] = max(hi - lo, 0);
+            const int lo = offsets[j - 1];
+            rows_s[j] = counts ? counts[j - 1] : max(offsets[j] - lo, 0);
             row0_s[j] = lo;
         }
     }

@@ -44,6 +44,7 @@ struct FinalizeArgs {
     float* P_out;             // [N]
     float* losses;            // [2]
     int* status;
+    int pad;                  // > 0: expert j's segment starts at a multiple of pad (offsets)
 };
 cudaError_t launch_route_finalize(const FinalizeArgs& a, cudaStream_t st);
 
@@ -52,9 +53,9 @@ cudaError_t launch_perm_scatter(const Dims& m, const int* topk_idx, const int* o
                                 const int* tile_base, int* perm_token, int* perm_slot,
                                 cudaStream_t st);
 
-// x_perm[perm_slot[t*K+k]] = u[t].
+// x_perm[perm_slot[t*K+k]] = u[t]; rows outside [0, row_limit) (default T*K') are corrupt.
 cudaError_t launch_gather(const Dims& m, const void* u, const int* perm_slot, void* x_perm,
-                          int* status, cudaStream_t st);
+                          int* status, cudaStream_t st, long row_limit = 0);
 
 // x_perm[r] = u[perm_token[r]] for r < offsets[N].
 cudaError_t launch_gather_rows(const Dims& m, const void* u, const int* offsets,
@@ -67,6 +68,68 @@ cudaError_t launch_expert_gemms(const Dims& m, const void* u, const void* x_perm
                                 const void* packed, const int* offsets, void* act_r, void* act_s,
                                 void* y_r, void* y_s, int* status, cudaStream_t st,
                                 cudaEvent_t mid_event);
+
+// One launch of the tensor-core grouped GEMM (bf16 in, fp32 accumulate, bf16 out): group 0 is a
+// dense group of T_shared rows (when has_shared), groups 1..n_routed the routed experts (rows
+// from offsets, or counts[j] rows at offsets[j] for padded segments). out = A * B^T, with
+// B = rows b_rows_per_expert * j ... of b_r for routed group j. epilogue 1: the SwiGLU of the
+// expert FFN (out = silu(gate) * up over the packed column pairs; pre_* receive the raw values
+// when set); 2: the SwiGLU backward (the product is d_act; with the saved values pre_* of the same
+// rows, out receives d_gate / d_up in packed order, row pitch ld); 0: a plain bf16 store.
+struct GroupedGemm {
+    const void *a_r, *a_s, *b_r, *b_s;
+    uint64_t a_rows_r, a_rows_s, k_r, k_s;   // A rows and K extents
+    uint64_t b_rows_r, b_rows_s;            // B total rows
+    int b_rows_per_expert, n_cols_r, n_cols_s;
+    void *out_r, *out_s;
+    int ld_r, ld_s;
+    void *pre_r, *pre_s;
+    int ld_pre_r, ld_pre_s;
+    int n_routed, has_shared, T_shared;
+    const int* offsets;
+    const int* counts;
+    long max_routed_rows;
+};
+cudaError_t run_grouped_gemm(const GroupedGemm& g, int epilogue, int* status, cudaStream_t st);
+
+// Weight-gradient GEMM C = A^T B summed over rows (see gemm_wgrad.cu). Group 0: dense over T rows
+// (A_s [T, M_s], B_s [T, N_s]); routed group j: rows poff[j] .. poff[j+1]-1 of A_r [rows_r, M_r],
+// B_r [rows_r, N_r] (padded, zero rows past the expert's count). mode 0 writes dW_down [E, d, I]
+// (out0), mode 1 dW_gate / dW_up [E, I, d] from packed rows (out0 / out1), mode 2 dense rows
+// [n_valid_rows, N_s] (out0). All fp32.
+struct WgradSpec {
+    const void *a_r, *b_r, *a_s, *b_s;
+    uint64_t rows_r;
+    int M_r, N_r, M_s, N_s;
+    int n_routed, has_shared, T;
+    const int* poff;
+    int mode;
+    float *out0, *out1;
+    int Ks, I, d, n_valid_rows;
+};
+cudaError_t launch_wgrad(const WgradSpec& s, int* status, cudaStream_t st);
+
+// ---- backward helpers (backward.cu) ----
+cudaError_t launch_pack_bwd(const Dims& m, const void* w_gate, const void* w_up,
+                            const void* w_down, void* packed_bwd, cudaStream_t st);
+cudaError_t launch_zero_pad_rows(const Dims& m, const int* poff, const int* counts, void* b0,
+                                 void* b1, int width, cudaStream_t st);
+cudaError_t launch_combine_bwd(const Dims& m, const void* dh, const void* y_r,
+                               const int* perm_slot, const float* gate, void* d_y, float* dgate,
+                               cudaStream_t st);
+cudaError_t launch_du_final(const Dims& m, const void* dh, const void* dx_s, const void* du_r,
+                            const void* dx, const int* perm_slot, float* du, cudaStream_t st);
+cudaError_t launch_transpose_centroids(const Dims& m, int n_pad, const void* e, void* eT,
+                                       cudaStream_t st);
+cudaError_t launch_dbias_reduce(int N, int n_tiles, const float* tile_dz, float* d_bias,
+                                cudaStream_t st);
+// Router backward (router_tc.cu): recomputes the affinities of each 128-token tile and writes
+// dz [T, n_pad] (bf16) = s * (ds - sum s ds), ds = gate gradient of the chosen ranks + the
+// balance-loss terms (a1 f_j + a2 f'_group(j)) / T, and per-tile column sums of dz [N][n_tiles].
+cudaError_t launch_router_bwd(const Dims& m, const void* u, const void* centroids,
+                              const float* bias, const int* topk_idx, const float* dgate,
+                              const int* counts, void* dz, float* tile_dz, int* status,
+                              cudaStream_t st);
 
 // h = u + y_s + sum_k gate * y_r[perm_slot].
 cudaError_t launch_combine(const Dims& m, const void* u, const void* y_r, const void* y_s,

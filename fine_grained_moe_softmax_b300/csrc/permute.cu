@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(1024) route_finalize_kernel(FinalizeArgs a) {
         int acc = 0;
         for (int j = 0; j < N; ++j) {
             off[j] = acc;
-            acc += total[j];
+            acc += a.pad > 0 ? (total[j] + a.pad - 1) / a.pad * a.pad : total[j];
         }
         off[N] = acc;
     }
@@ -183,13 +183,12 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(Dims m, const int* __
 
 // One warp per token: the row is read once (16-byte vectors) and written to its K' rows.
 __global__ void gather_kernel(Dims m, const uint4* __restrict__ u, const int* __restrict__ perm_slot,
-                              uint4* __restrict__ x_perm, int* status) {
+                              uint4* __restrict__ x_perm, int* status, long TK) {
     pdl_wait();
     pdl_trigger();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (warp >= m.T) return;
-    const int vec_per_row = m.d * m.elem() / 16;
-    const long TK = (long)m.T * m.K;
+    const int vec_per_row = m.d * m.elem() / 16;   // TK: rows of x_perm
     int rows[kMaxTopK];
 #pragma unroll
     for (int k = 0; k < kMaxTopK; ++k) rows[k] = k < m.K ? perm_slot[(size_t)warp * m.K + k] : -1;
@@ -275,13 +274,14 @@ cudaError_t launch_perm_scatter(const Dims& m, const int* topk_idx, const int* o
 }
 
 cudaError_t launch_gather(const Dims& m, const void* u, const int* perm_slot, void* x_perm,
-                          int* status, cudaStream_t st) {
+                          int* status, cudaStream_t st, long row_limit) {
+    const long rows = row_limit > 0 ? row_limit : (long)m.T * m.K;
     if (m.T == 0) return cudaSuccess;
     const int threads = 256, warps_per_block = threads / 32;
     const int blocks = (m.T + warps_per_block - 1) / warps_per_block;
     cudaError_t e = launch_pdl(gather_kernel, dim3(blocks), dim3(threads), 0, st, m,
                                static_cast<const uint4*>(u), perm_slot,
-                               static_cast<uint4*>(x_perm), status);
+                               static_cast<uint4*>(x_perm), status, rows);
     if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();

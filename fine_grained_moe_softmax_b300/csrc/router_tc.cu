@@ -39,6 +39,13 @@ struct RouterArgs {
     int* tile_counts;
     float* tile_psum;
     int* status;
+    // backward mode
+    const float* dgate;   // [T, K'] gradient of the chosen gates
+    const int* counts;    // [N'] selection counts of the batch (f_j)
+    __nv_bfloat16* dz;    // [T, n_pad] out
+    float* tile_dz;       // [N'][n_tiles] out: per-tile sums of dz
+    float a1, a2;
+    int D;
 };
 
 template <int KMAX>
@@ -177,7 +184,101 @@ __device__ __forceinline__ void route_tile(const RouterArgs& a, uint32_t tmem_la
     }
 }
 
-template <int KMAX>
+// Backward of the router for the tile's tokens (thread = token): with s = softmax(z) recomputed,
+// ds_j = aux_j + (gradient of the chosen gates through g = s or g = s / S), aux_j being the
+// balance-loss term (a1 f_j + a2 f'_group(j)) / T, and dz_j = s_j (ds_j - sum_m s_m ds_m).
+// dz is written as bf16 [T, n_pad] (zero past N'); its per-tile column sums (for the bias
+// gradient) go through the same fixed-order warp reduction as the affinity sums.
+__device__ __forceinline__ void route_tile_bwd(const RouterArgs& a, uint32_t tmem_lanes, float* zc,
+                                              int tile, int quarter, int lane, float* colsum,
+                                              const float* bias_s, const float* aux_s) {
+    const int N = a.N, K = a.K;
+    const int row = quarter * 32 + lane;
+    const int t = tile * RBM + row;
+    const bool valid = t < a.T;
+    const int n_chunks = a.n_pad / 32;
+    float zmax = -INFINITY;
+    for (int c = 0; c < n_chunks; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tmem_lanes + c * 32, v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int j = c * 32 + i;
+            if (j < N) {
+                const float z = __uint_as_float(v[i]) + bias_s[j];
+                zc[j * RBM + row] = z;
+                zmax = fmaxf(zmax, z);
+            }
+        }
+    }
+    float sum = 0.f;
+    for (int j = 0; j < N; ++j) {
+        const float e = __expf(zc[j * RBM + row] - zmax);
+        zc[j * RBM + row] = e;
+        sum += e;
+    }
+    const float inv = 1.0f / sum;
+    // chosen experts and the gradient of their gates with respect to their affinities
+    int cj[kMaxTopK];
+    float cs[kMaxTopK], cd[kMaxTopK];
+    float S = 0.f, w = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k) {
+        cj[k] = 0;
+        cs[k] = 0.f;
+        cd[k] = 0.f;
+        if (k < K && valid) {
+            int j = a.topk_idx[(size_t)t * K + k];
+            j = (j >= 0 && j < N) ? j : 0;
+            cj[k] = j;
+            cs[k] = zc[j * RBM + row] * inv;
+            cd[k] = a.dgate[(size_t)t * K + k];
+            S += cs[k];
+            w += cd[k] * cs[k];
+        }
+    }
+    float sds = 0.f;
+    for (int j = 0; j < N; ++j) sds += zc[j * RBM + row] * inv * aux_s[j];
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k) {
+        if (k < K && valid) {
+            cd[k] = a.renorm ? cd[k] / S - w / (S * S) : cd[k];   // chosen part of ds
+            sds += cs[k] * cd[k];
+        }
+    }
+    for (int j = 0; j < N; ++j) {
+        const float sj = zc[j * RBM + row] * inv;
+        zc[j * RBM + row] = valid ? sj * (aux_s[j] - sds) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k)
+        if (k < K && valid) zc[cj[k] * RBM + row] += cs[k] * cd[k];
+    for (int c = 0; c < n_chunks; ++c) {
+        float g[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int j = c * 32 + i;
+            g[i] = j < N ? zc[j * RBM + row] : 0.f;
+        }
+        if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(a.dz + (size_t)t * a.n_pad + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 o;
+                __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    o2[h] = __floats2bfloat162_rn(g[8 * q + 2 * h], g[8 * q + 2 * h + 1]);
+                dst[q] = o;
+            }
+        }
+        const float col = column_sums(g, lane);
+        colsum[quarter * kMaxRouted + c * 32 + lane] = col;
+    }
+}
+
+template <int KMAX, bool BWD>
 __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_constant__ RouterArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -192,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     float* colsum = reinterpret_cast<float*>(tmem_holder + 4);   // [4][kMaxRouted]
     int* hist = reinterpret_cast<int*>(colsum + 4 * kMaxRouted);  // [kMaxRouted]
     float* bias_s = reinterpret_cast<float*>(hist + kMaxRouted);  // [kMaxRouted]
+    float* aux_s = bias_s + kMaxRouted;                           // [kMaxRouted] (backward)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x;
@@ -220,6 +322,19 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     pdl_trigger();
     for (int j = threadIdx.x; j < kMaxRouted; j += blockDim.x)
         bias_s[j] = (a.bias && j < N) ? a.bias[j] : 0.f;
+    if constexpr (BWD) {   // balance-loss gradient per expert: (a1 f_j + a2 f'_group(j)) / T
+        const float Tf = (float)a.T, scale = (float)N / ((float)a.K * Tf);
+        const int gbase = N / a.D, extra = N % a.D;
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            const int g = j < extra * (gbase + 1) ? j / (gbase + 1)
+                                                  : extra + (j - extra * (gbase + 1)) / gbase;
+            const int first = g * gbase + (g < extra ? g : extra);
+            const int size = gbase + (g < extra ? 1 : 0);
+            float fs = 0.f;
+            for (int q = first; q < first + size; ++q) fs += scale * (float)a.counts[q];
+            aux_s[j] = (a.a1 * scale * (float)a.counts[j] + a.a2 * fs / (float)size) / Tf;
+        }
+    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -303,8 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
         if (ok) {
             ptx::tc_fence_after();
             // the MMAs are complete, so the TMA ring is idle and holds the per-token logit rows
-            route_tile<KMAX>(a, tb, reinterpret_cast<float*>(base), tile, quarter, lane, colsum,
-                             hist, bias_s);
+            if constexpr (BWD)
+                route_tile_bwd(a, tb, reinterpret_cast<float*>(base), tile, quarter, lane, colsum,
+                               bias_s, aux_s);
+            else
+                route_tile<KMAX>(a, tb, reinterpret_cast<float*>(base), tile, quarter, lane,
+                                 colsum, hist, bias_s);
             routed_here = true;
         }
         ptx::tc_fence_before();
@@ -312,10 +431,14 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
         if (routed_here) {
             const int n_tiles = gridDim.x;
             for (int j = et; j < N; j += 128) {
-                a.tile_psum[(size_t)j * n_tiles + tile] =
-                    ((colsum[j] + colsum[kMaxRouted + j]) + colsum[2 * kMaxRouted + j]) +
-                    colsum[3 * kMaxRouted + j];
-                a.tile_counts[(size_t)j * n_tiles + tile] = hist[j];
+                const float col = ((colsum[j] + colsum[kMaxRouted + j]) +
+                                   colsum[2 * kMaxRouted + j]) + colsum[3 * kMaxRouted + j];
+                if constexpr (BWD) {
+                    a.tile_dz[(size_t)j * n_tiles + tile] = col;
+                } else {
+                    a.tile_psum[(size_t)j * n_tiles + tile] = col;
+                    a.tile_counts[(size_t)j * n_tiles + tile] = hist[j];
+                }
             }
         }
     }
@@ -330,10 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
 
 }  // namespace
 
-cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids,
-                             const float* bias, int* topk_idx, float* topk_gate, int* tile_counts,
-                             float* tile_psum, int* status, cudaStream_t st) {
-    RouterArgs a{};
+static cudaError_t router_args(const Dims& m, const void* u, const void* centroids,
+                               const float* bias, RouterArgs& a) {
     a.n_pad = router_npad(m);
     if (!encode_bf16_map(&a.a, u, (uint64_t)m.T, (uint64_t)m.d, RBM) ||
         !encode_bf16_map(&a.b, centroids, (uint64_t)m.N, (uint64_t)m.d, a.n_pad))
@@ -350,21 +471,56 @@ cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids
     int cols = 32;
     while (cols < a.n_pad) cols *= 2;
     a.tmem_cols = cols;
-    a.topk_idx = topk_idx;
-    a.topk_gate = topk_gate;
-    a.tile_counts = tile_counts;
-    a.tile_psum = tile_psum;
-    a.status = status;
+    return cudaSuccess;
+}
+
+template <int KMAX, bool BWD>
+static cudaError_t launch_router_kernel(const Dims& m, const RouterArgs& a, cudaStream_t st) {
     const size_t smem = 1024 + (size_t)a.stages * a.stage_bytes + 8 * (2 * kMaxStages + 2) + 16 +
-                        4 * (4 * kMaxRouted + 2 * kMaxRouted);
+                        4 * (4 * kMaxRouted + 3 * kMaxRouted);
     const int n_tiles = (m.T + RBM - 1) / RBM;
-    auto kern = m.skip + m.K <= 8 ? router_tc_kernel<8> : router_tc_kernel<16>;
+    auto kern = router_tc_kernel<KMAX, BWD>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3(n_tiles), dim3(kThreads), smem, st, a);
     if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
+}
+
+cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids,
+                             const float* bias, int* topk_idx, float* topk_gate, int* tile_counts,
+                             float* tile_psum, int* status, cudaStream_t st) {
+    RouterArgs a{};
+    cudaError_t e = router_args(m, u, centroids, bias, a);
+    if (e != cudaSuccess) return e;
+    a.topk_idx = topk_idx;
+    a.topk_gate = topk_gate;
+    a.tile_counts = tile_counts;
+    a.tile_psum = tile_psum;
+    a.status = status;
+    return m.skip + m.K <= 8 ? launch_router_kernel<8, false>(m, a, st)
+                             : launch_router_kernel<16, false>(m, a, st);
+}
+
+cudaError_t launch_router_bwd(const Dims& m, const void* u, const void* centroids,
+                              const float* bias, const int* topk_idx, const float* dgate,
+                              const int* counts, void* dz, float* tile_dz, int* status,
+                              cudaStream_t st) {
+    if (m.T == 0) return cudaSuccess;
+    RouterArgs a{};
+    cudaError_t e = router_args(m, u, centroids, bias, a);
+    if (e != cudaSuccess) return e;
+    a.topk_idx = const_cast<int*>(topk_idx);
+    a.dgate = dgate;
+    a.counts = counts;
+    a.dz = static_cast<__nv_bfloat16*>(dz);
+    a.tile_dz = tile_dz;
+    a.a1 = m.a1;
+    a.a2 = m.a2;
+    a.D = m.D;
+    a.status = status;
+    return launch_router_kernel<8, true>(m, a, st);
 }
 
 }  // namespace moe

@@ -18,11 +18,12 @@ class MoELayer:
     ``cfg.T`` tokens per call.
 
     centroids [N', d], w_gate / w_up [K_s + N', I, d], w_down [K_s + N', d, I] (shared experts
-    first), logit_bias [N'] fp32 or None; all in the config's dtype (bias fp32).
+    first), logit_bias [N'] fp32 or None; all in the config's dtype (bias fp32). With
+    ``backward=True`` the transposed weight copies and the workspace of ``backward`` are set up too.
     """
 
     def __init__(self, cfg: B.MoEConfig, centroids, w_gate, w_up, w_down, logit_bias=None,
-                 device="cuda", stream=None):
+                 device="cuda", stream=None, backward: bool = False):
         self.cfg = copy.copy(cfg)
         self.device = torch.device(device)
         dt = cfg.torch_dtype()
@@ -35,6 +36,14 @@ class MoELayer:
         w_up = w_up.to(dev, dt).contiguous()
         w_down = w_down.to(dev, dt).contiguous()
         B.moe_pack_weights(self.cfg, w_gate, w_up, w_down, self.packed, stream)
+        self.packed_bwd = None
+        self.ws_bwd = None
+        if backward:
+            self.packed_bwd = torch.empty(B.moe_packed_backward_bytes(self.cfg), dtype=torch.uint8,
+                                          device=dev)
+            B.moe_pack_weights_backward(self.cfg, w_gate, w_up, w_down, self.packed_bwd, stream)
+            self.ws_bwd = torch.empty(max(B.moe_backward_workspace_bytes(self.cfg), 256),
+                                      dtype=torch.uint8, device=dev)
         if stream is None:
             torch.cuda.current_stream(dev).synchronize()
         else:
@@ -67,6 +76,27 @@ class MoELayer:
                             self.topk_idx[:T], self.topk_gate[:T], self.counts, self.f, self.P,
                             self.losses, self.ws, stream)
         return out
+
+    def backward(self, u: torch.Tensor, dh: torch.Tensor, stream=None) -> dict:
+        """Gradients of sum_t dh_t . h_t + L_ExpBal + L_DevBal (one moe_layer_backward call):
+        du, d_centroids, d_bias, dw_gate, dw_up, dw_down as fp32 device tensors."""
+        if self.ws_bwd is None:
+            raise RuntimeError("construct the layer with backward=True")
+        T = u.shape[0]
+        cfg = self.cfg_for(T)
+        c, dev = self.cfg, self.device
+        E = c.n_shared + c.n_routed
+        f32 = torch.float32
+        g = {"du": torch.empty(T, c.d, dtype=f32, device=dev),
+             "d_centroids": torch.empty(c.n_routed, c.d, dtype=f32, device=dev),
+             "d_bias": torch.empty(c.n_routed, dtype=f32, device=dev),
+             "dw_gate": torch.empty(E, c.inter, c.d, dtype=f32, device=dev),
+             "dw_up": torch.empty(E, c.inter, c.d, dtype=f32, device=dev),
+             "dw_down": torch.empty(E, c.d, c.inter, dtype=f32, device=dev)}
+        B.moe_layer_backward(cfg, u, self.centroids, self.logit_bias, self.packed,
+                             self.packed_bwd, dh, g["du"], g["d_centroids"], g["d_bias"],
+                             g["dw_gate"], g["dw_up"], g["dw_down"], self.ws_bwd, stream)
+        return g
 
     def capture(self, u: torch.Tensor):
         """Records one forward on the fixed input buffer ``u`` into a CUDA graph and returns

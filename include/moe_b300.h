@@ -148,6 +148,30 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
                       float* topk_gate, int32_t* counts, float* f, float* P, float* losses,
                       void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---- backward (training) ---- */
+
+/* The gradients of the training objective  sum_t dh_t . h_t + L_ExpBal + L_DevBal  with respect to
+ * the layer's inputs and parameters, with the expert selection and the selection counts held fixed
+ * (they are piecewise constant; the balance losses act through P_j, [P1] §方法细节; [P2] §2.3-2.4).
+ * bf16 layers only (fp32 configs return MOE_ERR_UNSUPPORTED). The call recomputes the forward pieces
+ * it needs from u and the weights, so it needs no state from a forward call.
+ *   packed_w from moe_pack_weights; packed_bwd from moe_pack_weights_backward (transposed copies
+ *   of the expert weights, moe_packed_backward_bytes(cfg) bytes);
+ *   dh [T, d] (layer dtype): upstream gradient of h;
+ *   du [T, d] fp32; d_centroids [N', d] fp32; d_bias [N'] fp32 (gradient of the logit bias, also
+ *   when logit_bias is NULL); dw_gate, dw_up [K_s+N', I, d] fp32; dw_down [K_s+N', d, I] fp32 —
+ *   all overwritten; experts without tokens (or disabled ones) receive zeros.
+ * ws: moe_backward_workspace_bytes(cfg) bytes, 256-byte aligned. */
+size_t moe_backward_workspace_bytes(const moe_config* cfg);
+size_t moe_packed_backward_bytes(const moe_config* cfg);
+int moe_pack_weights_backward(const moe_config* cfg, const void* w_gate, const void* w_up,
+                              const void* w_down, void* packed_bwd, moe_stream_t stream);
+int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroids,
+                       const float* logit_bias, const void* packed_w, const void* packed_bwd,
+                       const void* dh, float* du, float* d_centroids, float* d_bias,
+                       float* dw_gate, float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
 /* Waits for `stream`, then returns the device status word of `ws` (MOE_OK or a negative
  * moe_status), or MOE_ERR_CUDA if the wait itself failed. */
 int moe_device_status(const void* ws, moe_stream_t stream);

@@ -1,0 +1,98 @@
+"""GPU parity of the layer backward (moe_layer_backward through the C ABI) against the fp64
+oracle's backward, which is itself pinned by finite differences (test_oracle_backward.py).
+
+Objective: sum_t dh_t . h_t + L_ExpBal + L_DevBal with the expert selection and counts held fixed
+("DeepSeekMoE 论文解读" §方法细节). bf16 layers; every gradient tensor is compared by rel-L2."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+import oracle
+from oracle import OracleCfg
+from parity import NEAR_TIE, rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+def _shape(**kw):
+    base = dict(name="bwd", T=200, d=128, n_shared=1, n_routed=16, inter=32, top_k=4,
+                n_groups=4, dtype="bf16", seed=21, alpha1=0.01, alpha2=0.05)
+    base.update(kw)
+    return moe_inputs.MoEShape(**base)
+
+
+def _run(shape, dh_scale=1.0, bias=None):
+    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer
+    inputs = moe_inputs.make_inputs(shape)
+    if bias is not None:
+        inputs["bias"] = bias
+    cfg = OracleCfg.from_shape(shape)
+    r = oracle.route(cfg, inputs["u"], inputs["centroids"], inputs["bias"])
+    if (r["margin"] < NEAR_TIE).any():
+        pytest.skip("seeded input has a near-tie token")   # routing would be ambiguous
+    g = torch.Generator().manual_seed(shape.seed + 5)
+    dh = (torch.randn(shape.T, shape.d, generator=g) * dh_scale).to(torch.bfloat16)
+    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
+                     inputs["w_up"], inputs["w_down"], inputs["bias"], backward=True)
+    u = inputs["u"].to("cuda")
+    got = layer.backward(u, dh.to("cuda"))
+    torch.cuda.synchronize()
+    from fine_grained_moe_softmax_b300 import moe_device_status
+    assert moe_device_status(layer.ws_bwd) == 0
+    want = oracle.backward(cfg, inputs, dh.to(torch.float64).numpy(), r["counts"])
+    return {k: to_np(v) for k, v in got.items()}, want
+
+
+def _compare(got, want, keys=("du", "d_centroids", "d_bias", "dw_gate", "dw_up", "dw_down")):
+    errs = {k: rel_l2(got[k], want[k]) for k in keys}
+    bad = {k: v for k, v in errs.items() if not v <= TOL}
+    assert not bad, f"rel-L2 above {TOL}: {bad} (all: {errs})"
+    return errs
+
+
+@pytest.mark.parametrize("kw", [
+    dict(),
+    dict(renormalize=1),
+    dict(n_shared=2, top_k=2),
+    dict(n_shared=0),
+    dict(skip_top=2),
+    dict(drop_shared=1),
+    dict(T=129, n_routed=32, top_k=6, inter=48, n_groups=8),
+    dict(d=256, inter=64, T=300),
+    dict(inter=16, T=77, seed=23),          # half-chunk outputs everywhere
+    dict(inter=80, n_shared=3, seed=24),    # I % 32 == 16 with several shared experts
+])
+def test_backward_matches_oracle(kw):
+    got, want = _run(_shape(**kw))
+    _compare(got, want)
+
+
+def test_backward_of_balance_losses_alone():
+    """dh = 0: only L_ExpBal and L_DevBal drive the gradients (through the affinities), so the
+    expert weights get none and u / centroids / bias get the router's share."""
+    shape = _shape(alpha1=0.5, alpha2=0.8)
+    got, want = _run(shape, dh_scale=0.0)
+    for k in ("dw_gate", "dw_up", "dw_down"):
+        assert np.all(got[k] == 0)
+    _compare(got, want, keys=("du", "d_centroids", "d_bias"))
+
+
+def test_backward_2b_shape():
+    got, want = _run(moe_inputs.CONFIGS["2b_bf16"].with_(T=256))
+    _compare(got, want)
+
+
+def test_backward_zero_tokens():
+    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer
+    shape = _shape(T=16)
+    inputs = moe_inputs.make_inputs(shape)
+    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
+                     inputs["w_up"], inputs["w_down"], backward=True)
+    g = layer.backward(torch.empty(0, shape.d, dtype=torch.bfloat16, device="cuda"),
+                       torch.empty(0, shape.d, dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    for k in ("d_centroids", "d_bias", "dw_gate", "dw_up", "dw_down"):
+        assert torch.count_nonzero(g[k]) == 0

@@ -174,3 +174,14 @@ def test_graph_replay_matches_direct_calls():
     assert torch.equal(P_graph, layer.P)
     assert layer.device_status() == 0
 
+
+def test_layer_four_times_benchmark_tokens():
+    """The 16B-like layer at T = 65536 (4x the benchmark batch, about 5 GB of workspace): all
+    routing decisions, counts and statistics, and h on a sample that includes the last tile."""
+    shape = C["16b_bf16"]
+    T = 65536
+    inputs = moe_inputs.make_inputs(shape, T=T)
+    layer, u = run_layer(shape, inputs, T=T)
+    rng = np.random.default_rng(11)
+    sample = np.unique(np.concatenate([[0, T - 129, T - 1], rng.choice(T, 30, replace=False)]))
+    _compare_layer(shape, inputs, layer, u, tokens=sample)
