@@ -82,7 +82,8 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
     cudaStream_t st = (cudaStream_t)stream;
     const size_t E = (size_t)m.Ks + m.N, Id = (size_t)m.I * m.d;
     int* status = at<int>(ws, L.status);
-    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    // the status word and the tile counters of the three weight-gradient launches
+    if (cudaMemsetAsync(status, 0, 4 * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
     if (m.T == 0 || !m.shared_active()) {
         // no token gives a gradient to the disabled (or any, when T = 0) experts
         const size_t n_zero = m.T == 0 ? E : (size_t)m.Ks;
@@ -221,6 +222,7 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
         w.n_routed = 0;
         w.T = m.T;
         w.mode = 2;
+        w.tile_counter = status + 1;
         w.out0 = d_centroids;
         w.n_valid_rows = m.N;
         e = launch_wgrad(w, status, st);
@@ -287,6 +289,7 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
         w.T = m.T;
         w.poff = poff;
         w.mode = 0;
+        w.tile_counter = status + 2;
         w.out0 = dw_down;
         w.Ks = m.Ks;
         w.I = m.I;
@@ -309,6 +312,7 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
         w.T = m.T;
         w.poff = poff;
         w.mode = 1;
+        w.tile_counter = status + 3;
         w.out0 = dw_gate;
         w.out1 = dw_up;
         w.Ks = m.Ks;

@@ -6,14 +6,16 @@
 // over one dense shared group (all T tokens; the K_s shared experts side by side) and N' routed
 // groups (expert j: rows offsets[j] .. offsets[j+1]-1 of the permuted matrices).
 //
-// Kernel shape: persistent, one CTA per SM, 6 warps.
+// Kernel shape: persistent, one CTA per SM, 2 + EW warps.
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] (bf16, 128-byte swizzle) per
 //               stage into a STAGES-deep shared-memory ring.
 //   warp 1      allocates 2*BN TMEM columns; one thread issues tcgen05.mma (M=128, N=BN, K=16)
 //               into one of two fp32 accumulators, and commits stage releases and tile completion
 //               to mbarriers.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes 32*(w%4)..),
-//               SwiGLU or plain conversion to bf16, direct global stores of valid rows/columns.
+//   warps 2..   EW = 4 or 8 epilogue warps: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)..; with 8 warps two share each lane quarter and split its columns),
+//               SwiGLU (backward) or plain conversion to bf16, direct global stores of valid
+//               rows/columns.
 // Two accumulators let the epilogue of tile i overlap the main loop of tile i+1. Every wait on an
 // mbarrier is bounded in time; on expiry the kernel records MOE_ERR_TIMEOUT, stops issuing work,
 // drains what it issued and frees its TMEM before returning.
@@ -29,7 +31,7 @@
 
 namespace moe {
 
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -47,7 +49,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // swizzle, zero fill outside the matrix.
 bool encode_bf16_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
                      int box_rows) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn || rows == 0 || cols == 0) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
@@ -68,7 +70,13 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle row
-constexpr int kThreads = 192;
+
+// Epilogue warps per EPI (below): 4 suffice for the forward epilogues; the SwiGLU-backward epilogue
+// loads the saved gate/up values and does twice the arithmetic, and needs 8 to keep up.
+#ifndef MOE_GEMM_FWD_EPI_WARPS
+#define MOE_GEMM_FWD_EPI_WARPS 4
+#endif
+constexpr int epi_warps(int epi) { return epi == 2 ? 8 : MOE_GEMM_FWD_EPI_WARPS; }
 
 struct TcArgs {
     CUtensorMap a_r, a_s, b_r, b_s;
@@ -102,11 +110,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The saved gate/up values (packed layout) of intermediate columns col0 .. col0+31 of one row:
+// 64 contiguous bf16, of which the second 32 exist only when col0 + 16 < n_cols.
+__device__ __forceinline__ void load_pre_chunk(uint4 (&buf)[8], const __nv_bfloat16* row, int col0,
+                                               int n_cols, bool valid) {
+    if (!valid || col0 >= n_cols) return;
+    const uint4* src = reinterpret_cast<const uint4*>(row + 2 * col0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) buf[q] = src[q];
+    if (col0 + 16 < n_cols) {
+#pragma unroll
+        for (int q = 4; q < 8; ++q) buf[q] = src[q];
+    }
+}
+
 // EPI: 0 plain bf16 store; 1 SwiGLU of packed gate/up column pairs (expert FFN forward);
 // 2 SwiGLU backward: the accumulator is d_act, and with the saved gate/up values of the same rows
 // (pre, packed) the epilogue writes d_gate / d_up (packed) to out.
-template <int BN, int STAGES, int EPI>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcArgs args) {
+template <int BN, int STAGES, int EPI, int EW>
+__global__ void __launch_bounds__((2 + EW) * 32, 1)
+    gemm_tc_kernel(const __grid_constant__ TcArgs args) {
+    static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
     using S = Smem<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -135,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_addr(&tfull[a]), 1);
-            ptx::mbar_init(ptx::smem_addr(&tempty[a]), 4);
+            ptx::mbar_init(ptx::smem_addr(&tempty[a]), EW);
         }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
@@ -254,17 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
     } else {
         // --------------------------------------------------------------------- epilogue ----
+        constexpr int kChunks = BN / 32 / (EW / 4);     // 32-column chunks per warp and tile
         const int quarter = warp & 3;
+        const int c_first = ((warp - 2) >> 2) * kChunks;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const TileInfo ti = decode_tile(t, prefix, rows_s, row0_s, gt);
-            int ok = 1;
-            if (lane == 0)
-                ok = wait_phase(ptx::smem_addr(&tfull[acc]), acc_phase, abort_flag, args.status);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            ptx::tc_fence_after();
             const bool sh = ti.group == 0;
             const int r = ti.m_blk * BM + quarter * 32 + lane;     // row inside the group
             const bool valid = r < ti.m_rows;
@@ -272,13 +292,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const int ld = sh ? args.ld_s : args.ld_r;
             const int n_cols = sh ? args.n_cols_s : args.n_cols_r;
             const size_t orow = (size_t)(ti.row0 + r) * ld;
-            const uint32_t t_base = tmem + acc * BN + ((uint32_t)(quarter * 32) << 16);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int col0 = ti.n_blk * BN + c * 32;
+            const int col_base = ti.n_blk * BN + c_first * 32;
+            // EPI 2 reads the saved gate/up values of its rows one chunk ahead, the first chunk
+            // before the accumulator is ready, so that their DRAM latency overlaps the main loop
+            // and the previous chunk's arithmetic.
+            uint4 pre_buf[2][8];
+            const __nv_bfloat16* pre_row = nullptr;
+            if constexpr (EPI == 2) {
+                pre_row = (sh ? args.pre_s : args.pre_r) +
+                          (size_t)(ti.row0 + r) * (sh ? args.ld_pre_s : args.ld_pre_r);
+                load_pre_chunk(pre_buf[0], pre_row, col_base, n_cols, valid);
+            }
+            int ok = 1;
+            if (lane == 0)
+                ok = wait_phase(ptx::smem_addr(&tfull[acc]), acc_phase, abort_flag, args.status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t t_base =
+                tmem + acc * BN + c_first * 32 + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+                const int col0 = col_base + c * 32;
                 if (col0 >= n_cols) break;
                 uint32_t v[32];
                 ptx::tmem_ld_32x32b_x32(t_base + c * 32, v);
+                if constexpr (EPI == 2) {
+                    if (c + 1 < kChunks)
+                        load_pre_chunk(pre_buf[(c + 1) & 1], pre_row, col0 + 32, n_cols, valid);
+                }
                 ptx::tmem_ld_wait();
                 if (!valid) continue;
                 if constexpr (EPI == 1) {
@@ -308,19 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
                 } else if constexpr (EPI == 2) {
                     // columns col0 .. col0+31 are intermediate indices i; their gate/up values
-                    // sit in packed blocks col0/16 and col0/16 + 1 (32 values each)
-                    const __nv_bfloat16* pre = sh ? args.pre_s : args.pre_r;
-                    const size_t prow = (size_t)(ti.row0 + r) * (sh ? args.ld_pre_s : args.ld_pre_r);
+                    // are the packed blocks col0/16 and col0/16 + 1 (32 values each) of pre_buf
                     const int halves = col0 + 16 < n_cols ? 2 : 1;
+                    const uint4* raw = pre_buf[c & 1];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (h < halves) {
-                            const uint4* src = reinterpret_cast<const uint4*>(pre + prow + 2 * col0 +
-                                                                              32 * h);
-                            uint4 raw[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) raw[q] = src[q];
-                            const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(raw);
+                            const __nv_bfloat162* p2 =
+                                reinterpret_cast<const __nv_bfloat162*>(raw + 4 * h);
                             uint32_t o[16];
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
@@ -328,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                                 const float2 u2 = __bfloat1622float2(p2[8 + q]);   // up
                                 const float da0 = __uint_as_float(v[16 * h + 2 * q]);
                                 const float da1 = __uint_as_float(v[16 * h + 2 * q + 1]);
-                                const float s0 = 1.0f / (1.0f + __expf(-g2.x));
-                                const float s1 = 1.0f / (1.0f + __expf(-g2.y));
+                                const float s0 = __fdividef(1.0f, 1.0f + __expf(-g2.x));
+                                const float s1 = __fdividef(1.0f, 1.0f + __expf(-g2.y));
                                 o[q] = pack_bf16x2(da0 * u2.x * s0 * (1.0f + g2.x * (1.0f - s0)),
                                                    da1 * u2.y * s1 * (1.0f + g2.y * (1.0f - s1)));
                                 o[8 + q] = pack_bf16x2(da0 * g2.x * s0, da1 * g2.y * s1);
@@ -377,11 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 template <int BN, int STAGES, int EPI>
 cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
     using S = Smem<BN, STAGES>;
-    auto kern = gemm_tc_kernel<BN, STAGES, EPI>;
+    constexpr int EW = epi_warps(EPI);
+    auto kern = gemm_tc_kernel<BN, STAGES, EPI, EW>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), S::total);
     if (e != cudaSuccess) return e;
     const int grid = max(1, min(sm_count(), max_tiles));
-    e = launch_pdl(kern, dim3(grid), dim3(kThreads), S::total, st, args);
+    e = launch_pdl(kern, dim3(grid), dim3((2 + EW) * 32), S::total, st, args);
     if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();

@@ -13,6 +13,17 @@
 // bytes; the MMA descriptors step through 16-row K slices (2 atoms) and across the 64-column boxes
 // with the leading-byte offset. Same warp roles, TMEM double buffering and bounded waits as
 // gemm_tc.cu.
+//
+// Tiles are claimed dynamically: the dense group's tiles reduce over all T rows and run an order
+// of magnitude longer than a routed expert's, so a static round-robin leaves some SMs one long
+// tile behind. The producer takes the next tile index from a global counter (zeroed by the
+// caller before the launch; one claim ahead of the tile it loads) and hands each index to the MMA
+// and epilogue warps through a small shared-memory ring; an index >= the tile count ends all roles.
+//
+// The fp32 results leave through TMA bulk stores: each epilogue warp stages its 32 rows x 16
+// columns (a 2 KB box, 64-byte swizzle, so the thread-per-row writes are free of bank conflicts)
+// in one of two shared buffers and one lane stores the box through a 3D tensor map
+// [experts][rows][columns] of the output, whose extents clip rows and columns outside an expert.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -26,6 +37,12 @@ namespace {
 
 constexpr int WBM = 128, WBN = 256, WBK = 64, WSTAGES = 4, kWThreads = 192;
 constexpr uint32_t kABytes = WBM * WBK * 2, kBBytes = WBN * WBK * 2, kBox = 64 * 64 * 2;
+constexpr int kTileRing = 8;   // tile indices in flight between the producer and the consumers
+constexpr uint32_t kStageBytes = 2 * 2 * 32 * 16 * 4;   // per epilogue warp: 2 buffers x 2 halves
+constexpr size_t kWgradSmem = 1024 + (size_t)WSTAGES * (kABytes + kBBytes) + 4 * kStageBytes +
+                              8 * (2 * WSTAGES + 5 + 2 * kTileRing) + 16 + 4 * kTileRing +
+                              4 * (kMaxRouted + 2);
+static_assert(kWgradSmem <= 232448, "shared memory of the weight-gradient kernel");
 
 struct WgArgs {
     CUtensorMap a_r, a_s, b_r, b_s;   // [rows, M] / [rows, N], box [64 rows x 64 columns]
@@ -34,9 +51,9 @@ struct WgArgs {
     int M_r, N_r, M_s, N_s;           // C extents per group kind
     int mt_r, nt_r, mt_s, nt_s;       // tiles per group
     int mode;                         // 0: dW_down, 1: dW_gate / dW_up, 2: dense rows
-    float* out0;
-    float* out1;
+    CUtensorMap out_map0, out_map1;   // fp32 outputs as [experts][rows][columns], 16-column boxes
     int Ks, I, d, n_valid_rows;
+    int* tile_counter;                // zero at launch
     int* status;
 };
 
@@ -80,55 +97,25 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo) 
     return desc;
 }
 
-// Stores 16 consecutive columns (c0 .. c0+15) of C row m for the tile's group.
-__device__ __forceinline__ void store16(const WgArgs& a, int group, int m, int c0,
-                                        const float* v) {
-    float* dst = nullptr;
-    if (a.mode == 0) {        // dW_down [E, d, I]: row m = model column n, column = intermediate
-        int e, i;
-        if (group == 0) {
-            e = c0 / a.I;
-            i = c0 % a.I;
-        } else {
-            e = a.Ks + group - 1;
-            i = c0;
-        }
-        dst = a.out0 + ((size_t)e * a.d + m) * a.I + i;
-    } else if (a.mode == 1) { // dW_gate / dW_up [E, I, d]: row m = packed gate/up row
-        const int ig = 16 * (m / 32) + (m & 15);
-        int e, i;
-        if (group == 0) {
-            e = ig / a.I;
-            i = ig % a.I;
-        } else {
-            e = a.Ks + group - 1;
-            i = ig;
-        }
-        dst = ((m & 31) < 16 ? a.out0 : a.out1) + ((size_t)e * a.I + i) * a.d + c0;
-    } else {                  // dense [rows, N]
-        if (m >= a.n_valid_rows) return;
-        dst = a.out0 + (size_t)m * a.N_s + c0;
-    }
-    float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-
 __global__ void __launch_bounds__(kWThreads, 1) wgrad_kernel(const __grid_constant__ WgArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* a_ring = base;
     uint8_t* b_ring = base + WSTAGES * kABytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + WSTAGES * (kABytes + kBBytes));
+    uint8_t* staging = base + WSTAGES * (kABytes + kBBytes);   // [4 warps][kStageBytes]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + 4 * kStageBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + WSTAGES;
     uint64_t* tfull = bars + 2 * WSTAGES;
     uint64_t* tempty = bars + 2 * WSTAGES + 2;
     uint64_t* drain = bars + 2 * WSTAGES + 4;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* tile_full = drain + 1;             // [kTileRing]: an index was published
+    uint64_t* tile_empty = tile_full + kTileRing; // [kTileRing]: MMA + 4 epilogue warps read it
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tile_empty + kTileRing);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    int* poff_s = reinterpret_cast<int*>(tmem_holder + 4);   // [n_routed + 1]
+    volatile int* tile_idx = reinterpret_cast<volatile int*>(tmem_holder + 4);   // [kTileRing]
+    int* poff_s = reinterpret_cast<int*>(tmem_holder + 4 + kTileRing);          // [n_routed + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -141,6 +128,10 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_kernel(const __grid_consta
             ptx::mbar_init(ptx::smem_addr(&tempty[b]), 4);
         }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
+        for (int r = 0; r < kTileRing; ++r) {
+            ptx::mbar_init(ptx::smem_addr(&tile_full[r]), 1);
+            ptx::mbar_init(ptx::smem_addr(&tile_empty[r]), 5);
+        }
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -149,6 +140,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_kernel(const __grid_consta
         ptx::prefetch_tmap(&a.a_s);
         ptx::prefetch_tmap(&a.b_r);
         ptx::prefetch_tmap(&a.b_s);
+        ptx::prefetch_tmap(&a.out_map0);
+        if (a.mode == 1) ptx::prefetch_tmap(&a.out_map1);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_holder), 2 * WBN);
@@ -165,10 +158,25 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_kernel(const __grid_consta
 
     if (warp == 0) {
         if (lane == 0) {   // ------------------------------------------------- TMA producer
-            int stage = 0, issued = 0;
-            uint32_t phase = 0;
+            int stage = 0, issued = 0, slot = 0;
+            uint32_t phase = 0, slot_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            int next_t = atomicAdd(a.tile_counter, 1);
+            while (ok) {
+                const int t = next_t;
+                if (!wait_phase(ptx::smem_addr(&tile_empty[slot]), slot_phase ^ 1, abort_flag,
+                                a.status)) {
+                    ok = false;
+                    break;
+                }
+                tile_idx[slot] = t;
+                ptx::mbar_arrive(ptx::smem_addr(&tile_full[slot]));
+                if (++slot == kTileRing) {
+                    slot = 0;
+                    slot_phase ^= 1;
+                }
+                if (t >= total) break;
+                next_t = atomicAdd(a.tile_counter, 1);
                 const WTile w = decode(t, a, poff_s);
                 const bool sh = w.group == 0;
                 const CUtensorMap* am = sh ? &a.a_s : &a.a_r;
@@ -210,10 +218,19 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_kernel(const __grid_consta
     } else if (warp == 1) {
         if (lane == 0) {   // -------------------------------------------------- MMA issuer
             const uint32_t idesc = ptx::idesc_bf16_f32(WBM, WBN) | (1u << 15) | (1u << 16);
-            int stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, acc = 0, slot = 0;
+            uint32_t phase = 0, acc_phase = 0, slot_phase = 0;
             bool ok = true, any = false;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            while (ok) {
+                if (!wait_phase(ptx::smem_addr(&tile_full[slot]), slot_phase, abort_flag, a.status))
+                    break;
+                const int t = tile_idx[slot];
+                ptx::mbar_arrive(ptx::smem_addr(&tile_empty[slot]));
+                if (++slot == kTileRing) {
+                    slot = 0;
+                    slot_phase ^= 1;
+                }
+                if (t >= total) break;
                 const WTile w = decode(t, a, poff_s);
                 if (!wait_phase(ptx::smem_addr(&tempty[acc]), acc_phase ^ 1, abort_flag,
                                 a.status))
@@ -254,9 +271,23 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_kernel(const __grid_consta
         }
     } else {               // ---------------------------------------------------- epilogue
         const int quarter = warp & 3;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        uint8_t* my_stage = staging + (warp - 2) * kStageBytes;
+        int acc = 0, slot = 0, sbuf = 0;
+        uint32_t acc_phase = 0, slot_phase = 0;
+        while (true) {
+            int t = total;
+            if (lane == 0) {
+                if (wait_phase(ptx::smem_addr(&tile_full[slot]), slot_phase, abort_flag, a.status)) {
+                    t = tile_idx[slot];
+                    ptx::mbar_arrive(ptx::smem_addr(&tile_empty[slot]));
+                }
+            }
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (++slot == kTileRing) {
+                slot = 0;
+                slot_phase ^= 1;
+            }
+            if (t >= total) break;
             const WTile w = decode(t, a, poff_s);
             int ok = 1;
             if (lane == 0)
@@ -266,27 +297,58 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_kernel(const __grid_consta
             ptx::tc_fence_after();
             const bool sh = w.group == 0;
             const int M = sh ? a.M_s : a.M_r, Ncols = sh ? a.N_s : a.N_r;
-            const int m = w.m_blk * WBM + quarter * 32 + lane;
+            const int m0 = w.m_blk * WBM + quarter * 32;        // first C row of this warp
             const uint32_t t_base = tmem + acc * WBN + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < WBN / 32; ++c) {
                 const int col0 = w.n_blk * WBN + c * 32;
                 if (col0 >= Ncols) break;
-                float v[32];
+                uint32_t v[32];
                 if (w.k_blocks > 0) {
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(t_base + c * 32, r);
+                    ptx::tmem_ld_32x32b_x32(t_base + c * 32, v);
                     ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.f;   // an expert without tokens
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;   // an expert without tokens
                 }
-                if (m < M) {
-                    store16(a, w.group, m, col0, v);
-                    if (col0 + 16 < Ncols) store16(a, w.group, m, col0 + 16, v + 16);
+                if (m0 >= M) continue;   // warp-uniform: rows past the C extent
+                // the buffer written two chunks ago must have been read by its stores
+                if (lane == 0) ptx::bulk_wait_read<1>();
+                __syncwarp();
+                uint8_t* buf = my_stage + sbuf * (kStageBytes / 2);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int pos = h * 2048 + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
+                        *reinterpret_cast<uint4*>(buf + pos) =
+                            make_uint4(v[16 * h + 4 * q], v[16 * h + 4 * q + 1],
+                                       v[16 * h + 4 * q + 2], v[16 * h + 4 * q + 3]);
+                    }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t sb = ptx::smem_addr(buf);
+                    for (int h = 0; h < 2; ++h) {
+                        const int cc = col0 + 16 * h;   // first C column of the box
+                        if (cc >= Ncols) break;
+                        if (a.mode == 1) {   // packed rows m0.. -> 16 gate rows, 16 up rows
+                            const int ig = 16 * (m0 / 32);
+                            const int e = sh ? ig / a.I : a.Ks + w.group - 1;
+                            const int i = sh ? ig % a.I : ig;
+                            ptx::tma_store_3d(&a.out_map0, sb + h * 2048, cc, i, e);
+                            ptx::tma_store_3d(&a.out_map1, sb + h * 2048 + 1024, cc, i, e);
+                        } else if (a.mode == 0) {   // C rows = model columns, C columns = i
+                            const int e = sh ? cc / a.I : a.Ks + w.group - 1;
+                            const int i = sh ? cc % a.I : cc;
+                            ptx::tma_store_3d(&a.out_map0, sb + h * 2048, i, m0, e);
+                        } else if (m0 < a.n_valid_rows) {   // dense: rows past N' are padding
+                            ptx::tma_store_3d(&a.out_map0, sb + h * 2048, cc, m0, 0);
+                        }
+                    }
+                    ptx::bulk_commit();
                 }
+                sbuf ^= 1;
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -296,6 +358,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_kernel(const __grid_consta
                 acc_phase ^= 1;
             }
         }
+        if (lane == 0) ptx::bulk_wait_all();   // the stores read shared memory until they finish
     }
 
     ptx::tc_fence_before();
@@ -309,6 +372,20 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_kernel(const __grid_consta
 // [rows, cols] bf16 row-major as an MN-major operand: box of 64 rows x 64 columns.
 bool encode_mn_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols) {
     return encode_bf16_map(map, ptr, rows, cols, 64);
+}
+
+// fp32 [experts, rows, cols] row-major output with a [1 x box_rows x 16] box, 64-byte swizzle.
+bool encode_out_map(CUtensorMap* map, float* ptr, uint64_t experts, uint64_t rows, uint64_t cols,
+                    int box_rows) {
+    auto fn = tensor_map_encoder();
+    if (!fn || !ptr || experts == 0 || rows == 0 || cols == 0) return false;
+    cuuint64_t dims[3] = {cols, rows, experts};
+    cuuint64_t strides[2] = {cols * 4, rows * cols * 4};
+    cuuint32_t box[3] = {16u, (cuuint32_t)box_rows, 1u};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -341,17 +418,26 @@ cudaError_t launch_wgrad(const WgradSpec& s, int* status, cudaStream_t st) {
     a.mt_s = (s.M_s + WBM - 1) / WBM;
     a.nt_s = (s.N_s + WBN - 1) / WBN;
     a.mode = s.mode;
-    a.out0 = s.out0;
-    a.out1 = s.out1;
+    const uint64_t E = (uint64_t)s.Ks + s.n_routed;
+    bool maps_ok;
+    if (s.mode == 0)
+        maps_ok = encode_out_map(&a.out_map0, s.out0, E, s.d, s.I, 32);
+    else if (s.mode == 1)
+        maps_ok = encode_out_map(&a.out_map0, s.out0, E, s.I, s.d, 16) &&
+                  encode_out_map(&a.out_map1, s.out1, E, s.I, s.d, 16);
+    else
+        maps_ok = encode_out_map(&a.out_map0, s.out0, 1, s.n_valid_rows, s.N_s, 32);
+    if (!maps_ok) return cudaErrorInvalidValue;
     a.Ks = s.Ks;
     a.I = s.I;
     a.d = s.d;
     a.n_valid_rows = s.n_valid_rows;
+    a.tile_counter = s.tile_counter;
     a.status = status;
     const long total = (long)(s.has_shared ? a.mt_s * a.nt_s : 0) + (long)s.n_routed * a.mt_r * a.nt_r;
     if (total == 0) return cudaSuccess;
-    const size_t smem = 1024 + (size_t)WSTAGES * (kABytes + kBBytes) + 8 * (2 * WSTAGES + 5) + 16 +
-                        4 * (kMaxRouted + 2);
+    if (!s.tile_counter) return cudaErrorInvalidValue;
+    const size_t smem = kWgradSmem;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(wgrad_kernel), smem);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<long>(total, sm_count());

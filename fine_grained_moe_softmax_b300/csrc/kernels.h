@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -21,6 +22,8 @@ cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids
                              const float* bias, int* topk_idx, float* topk_gate, int* tile_counts,
                              float* tile_psum, int* status, cudaStream_t st);
 
+// The driver's tensor-map encoder (resolved once through the runtime), or null.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // Row-major bf16 [rows, cols] as a 2D TMA map, box [box_rows x 64], 128-byte swizzle.
 bool encode_bf16_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
                      int box_rows);
@@ -106,6 +109,7 @@ struct WgradSpec {
     int mode;
     float *out0, *out1;
     int Ks, I, d, n_valid_rows;
+    int* tile_counter;   // device int, zero when the launch starts (dynamic tile claims)
 };
 cudaError_t launch_wgrad(const WgradSpec& s, int* status, cudaStream_t st);
 
