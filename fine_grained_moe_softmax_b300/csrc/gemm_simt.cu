@@ -108,6 +108,7 @@ cudaError_t run_simt(const Dims& m, SimtArgs a, cudaStream_t st) {
     a.gt.n_groups = 1 + m.N;
     a.gt.has_shared = m.shared_active();
     a.gt.T = m.T;
+    a.gt.max_rows_r = m.T * m.K;
     a.gt.n_tiles_r = (a.n_out_r + SB - 1) / SB;
     a.gt.n_tiles_s = m.shared_active() ? (a.n_out_s + SB - 1) / SB : 0;
     cudaError_t e = launch_pdl(gemm_simt_kernel<GATEUP>, dim3(4 * sm_count()), dim3(256), 0, st, a);

@@ -177,7 +177,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
     }
     pdl_wait();
     pdl_trigger();
-    build_tile_prefix<BM>(prefix, rows_s, row0_s, args.offsets, gt, args.counts);   // syncs
+    build_tile_prefix<BM>(prefix, rows_s, row0_s, args.offsets, gt, args.counts,
+                          args.status);   // syncs
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -465,6 +466,7 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     a.gt.n_groups = 1 + g.n_routed;
     a.gt.has_shared = shared;
     a.gt.T = g.T_shared;
+    a.gt.max_rows_r = (int)std::min<uint64_t>(g.a_rows_r, INT32_MAX);
     a.gt.n_tiles_r = (g.n_cols_r + bn - 1) / bn;
     a.gt.n_tiles_s = shared ? (g.n_cols_s + bn - 1) / bn : 0;
     a.k_blocks_r = (int)((g.k_r + BK - 1) / BK);

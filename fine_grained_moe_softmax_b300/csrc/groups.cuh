@@ -17,6 +17,7 @@ struct GroupTiles {
     int T;             // rows of the shared group
     int n_tiles_r;     // column tiles of a routed group
     int n_tiles_s;     // column tiles of the shared group
+    int max_rows_r;    // rows of the routed A / output matrices
 };
 
 struct TileInfo {
@@ -28,20 +29,29 @@ struct TileInfo {
 
 // Fills prefix[0 .. n_groups] (shared memory) from offsets; every thread of the CTA must call it.
 // With `counts`, routed expert j has counts[j] rows starting at offsets[j] (padded segments);
-// otherwise its rows are offsets[j] .. offsets[j+1]-1.
+// otherwise its rows are offsets[j] .. offsets[j+1]-1. A group reaching outside
+// [0, gt.max_rows_r) (corrupt offsets from a caller) is cut to the rows inside and reported as
+// MOE_ERR_CORRUPT_INPUT, so no tile can address rows outside the routed matrices.
 template <int BM>
 __device__ __forceinline__ void build_tile_prefix(int* prefix, int* rows_s, int* row0_s,
                                                   const int* __restrict__ offsets,
                                                   const GroupTiles& gt,
-                                                  const int* __restrict__ counts = nullptr) {
+                                                  const int* __restrict__ counts = nullptr,
+                                                  int* status = nullptr) {
     const int N = gt.n_groups - 1;
     for (int j = threadIdx.x; j <= N; j += blockDim.x) {
         if (j == 0) {
             rows_s[0] = gt.has_shared ? gt.T : 0;
             row0_s[0] = 0;
         } else {
-            const int lo = offsets[j - 1];
-            rows_s[j] = counts ? counts[j - 1] : max(offsets[j] - lo, 0);
+            int lo = offsets[j - 1];
+            int rows = counts ? counts[j - 1] : offsets[j] - lo;
+            if (lo < 0 || lo > gt.max_rows_r || rows < 0 || rows > gt.max_rows_r - lo) {
+                if (status) set_status(status, MOE_ERR_CORRUPT_INPUT);
+                lo = min(max(lo, 0), gt.max_rows_r);
+                rows = min(max(rows, 0), gt.max_rows_r - lo);
+            }
+            rows_s[j] = rows;
             row0_s[j] = lo;
         }
     }

@@ -187,6 +187,46 @@ def test_combine_reports_bad_rows():
     assert st.status() == 0
 
 
+@pytest.mark.parametrize("name", ["2b_bf16", "tiny_f32"])
+def test_ffn_reports_bad_token_rows(name):
+    """Token indices outside [0, T) in perm_token are reported by the gather and never
+    dereferenced; every other routed row comes out bit for bit as before."""
+    st = Stages(C[name], 300)
+    st.route()
+    st.permute()
+    st.pack()
+    st.ffn()
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    ref = st.y_r.clone()
+    st.perm_token[11] = st.T + 7
+    st.perm_token[12] = -2
+    st.ffn()
+    torch.cuda.synchronize()
+    assert st.status() == -6
+    keep = torch.ones(st.y_r.shape[0], dtype=torch.bool, device=st.y_r.device)
+    keep[11] = keep[12] = False
+    assert torch.equal(st.y_r[keep], ref[keep])
+
+
+def test_ffn_reports_bad_offsets():
+    """Offsets that run past the T*K' routed rows or decrease are cut to the rows that exist and
+    reported; a following call with good offsets is clean."""
+    st = Stages(C["2b_bf16"], 300)
+    st.route()
+    st.permute()
+    st.pack()
+    bad = st.offsets.clone()
+    bad[-1] += 500
+    bad[5] = bad[6] + 3
+    st.moe.moe_expert_ffn(st.cfg, st.u, st.packed, bad, st.perm_token, st.y_r, st.y_s, st.ws)
+    torch.cuda.synchronize()
+    assert st.status() == -6
+    st.ffn()
+    torch.cuda.synchronize()
+    assert st.status() == 0
+
+
 def test_stage_errors_raise():
     import fine_grained_moe_softmax_b300 as moe
     st = Stages(C["tiny_f32"], 64)
