@@ -14,8 +14,10 @@
 //               to mbarriers.
 //   warps 2..   EW = 4 or 8 epilogue warps: tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32*(w%4)..; with 8 warps two share each lane quarter and split its columns),
-//               SwiGLU (backward) or plain conversion to bf16, direct global stores of valid
-//               rows/columns.
+//               SwiGLU (backward) or plain conversion to bf16. The plain epilogue stages each
+//               warp's 32 rows x 32 columns in shared memory (64-byte swizzle) and writes them with
+//               a TMA bulk store; the others (and a warp whose rows cross the end of a group) store
+//               valid rows/columns directly.
 // Two accumulators let the epilogue of tile i overlap the main loop of tile i+1. Every wait on an
 // mbarrier is bounded in time; on expiry the kernel records MOE_ERR_TIMEOUT, stops issuing work,
 // drains what it issued and frees its TMEM before returning.
@@ -61,6 +63,21 @@ bool encode_bf16_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t 
            CUDA_SUCCESS;
 }
 
+// Row-major bf16 output [rows, cols] with row stride ld (elements) as a 2D TMA map for stores,
+// box [32 rows x 32 columns], 64-byte swizzle; columns >= cols and rows >= rows are clipped.
+static bool encode_out_map(CUtensorMap* map, void* ptr, uint64_t rows, uint64_t cols,
+                           uint64_t ld) {
+    auto fn = tensor_map_encoder();
+    if (!fn || !ptr || rows == 0 || cols == 0) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_expert_gemms_simt(const Dims& m, const void* u, const void* x_perm,
                                      const void* packed, const int* offsets, void* act_r,
                                      void* act_s, void* y_r, void* y_s, cudaStream_t st,
@@ -80,6 +97,7 @@ constexpr int epi_warps(int epi) { return epi == 2 ? 8 : MOE_GEMM_FWD_EPI_WARPS;
 
 struct TcArgs {
     CUtensorMap a_r, a_s, b_r, b_s;
+    CUtensorMap o_r, o_s;         // EPI 0: outputs [rows, n_cols] with a [32 x 32] box
     const int* offsets;
     const int* counts;            // optional: rows per routed group (padded segments)
     GroupTiles gt;
@@ -95,14 +113,20 @@ struct TcArgs {
     int* status;
 };
 
-template <int BN, int STAGES>
+// EPI 0 output staging: per epilogue warp two 2 KB boxes (32 rows x 32 bf16)
+constexpr uint32_t kOutBox = 32 * 32 * 2;
+constexpr uint32_t staging_bytes(int epi) { return epi == 0 ? 4 * 2 * kOutBox : 0; }
+
+template <int BN, int STAGES, int EPI>
 struct Smem {
     static constexpr uint32_t a_bytes = BM * BK * 2;
     static constexpr uint32_t b_bytes = BN * BK * 2;
     static constexpr uint32_t ring = STAGES * (a_bytes + b_bytes);
+    static constexpr uint32_t staging = staging_bytes(EPI);
     static constexpr uint32_t bars = 8 * (2 * STAGES + 5);
     static constexpr uint32_t tables = 4 * (3 * (kMaxRouted + 2));
-    static constexpr uint32_t total = 1024 + ring + bars + 16 + tables;
+    static constexpr uint32_t total = 1024 + ring + staging + bars + 16 + tables;
+    static_assert(total <= 232448, "shared memory of the expert GEMM");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -131,21 +155,22 @@ template <int BN, int STAGES, int EPI, int EW>
 __global__ void __launch_bounds__((2 + EW) * 32, 1)
     gemm_tc_kernel(const __grid_constant__ TcArgs args) {
     static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
-    using S = Smem<BN, STAGES>;
+    using S = Smem<BN, STAGES, EPI>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* a_ring = base;
     uint8_t* b_ring = base + STAGES * S::a_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + S::ring);
+    uint8_t* staging = base + S::ring;   // [4 warps][2][kOutBox] (EPI 0)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + S::ring + S::staging);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = bars + 2 * STAGES + 2;
     uint64_t* drain = bars + 2 * STAGES + 4;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + S::ring + S::bars);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base + S::ring + S::staging + S::bars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    int* prefix = reinterpret_cast<int*>(base + S::ring + S::bars + 16);
+    int* prefix = reinterpret_cast<int*>(base + S::ring + S::staging + S::bars + 16);
     int* rows_s = prefix + (kMaxRouted + 2);
     int* row0_s = rows_s + (kMaxRouted + 2);
 
@@ -170,6 +195,10 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         ptx::prefetch_tmap(&args.a_s);
         ptx::prefetch_tmap(&args.b_r);
         ptx::prefetch_tmap(&args.b_s);
+        if constexpr (EPI == 0) {
+            ptx::prefetch_tmap(&args.o_r);
+            ptx::prefetch_tmap(&args.o_s);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_holder), 2 * BN);
@@ -282,6 +311,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         constexpr int kChunks = BN / 32 / (EW / 4);     // 32-column chunks per warp and tile
         const int quarter = warp & 3;
         const int c_first = ((warp - 2) >> 2) * kChunks;
+        uint8_t* my_stage = staging + (EPI == 0 ? (warp - 2) * 2 * kOutBox : 0);
+        int sbuf = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -294,6 +325,9 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             const int n_cols = sh ? args.n_cols_s : args.n_cols_r;
             const size_t orow = (size_t)(ti.row0 + r) * ld;
             const int col_base = ti.n_blk * BN + c_first * 32;
+            // all 32 rows of this warp lie inside the group: the box store cannot reach rows of
+            // the next group
+            const bool box_store = EPI == 0 && ti.m_blk * BM + quarter * 32 + 32 <= ti.m_rows;
             // EPI 2 reads the saved gate/up values of its rows one chunk ahead, the first chunk
             // before the accumulator is ready, so that their DRAM latency overlaps the main loop
             // and the previous chunk's arithmetic.
@@ -383,13 +417,33 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
 #pragma unroll
                     for (int q = 0; q < 16; ++q)
                         o[q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-                    uint4* dst = reinterpret_cast<uint4*>(out + orow + col0);
-                    // widths are multiples of 16: the second half of a chunk may lie past the end
-                    const int halves = col0 + 16 < n_cols ? 2 : 1;
+                    if (box_store) {
+                        // the buffer written two chunks ago must have been read by its store
+                        if (lane == 0) ptx::bulk_wait_read<1>();
+                        __syncwarp();
+                        uint8_t* buf = my_stage + sbuf * kOutBox;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (q < 2 * halves)
-                            dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4*>(buf + lane * 64 +
+                                                      ((q ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {   // columns past n_cols are clipped by the map
+                            ptx::tma_store_2d(sh ? &args.o_s : &args.o_r, ptx::smem_addr(buf), col0,
+                                              ti.row0 + ti.m_blk * BM + quarter * 32);
+                            ptx::bulk_commit();
+                        }
+                        sbuf ^= 1;
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(out + orow + col0);
+                        // widths are multiples of 16: the second half of a chunk may lie past the end
+                        const int halves = col0 + 16 < n_cols ? 2 : 1;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (q < 2 * halves)
+                                dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                    }
                 }
             }
             ptx::tc_fence_before();
@@ -399,6 +453,9 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                 acc = 0;
                 acc_phase ^= 1;
             }
+        }
+        if constexpr (EPI == 0) {   // the box stores read shared memory until they finish
+            if (lane == 0) ptx::bulk_wait_all();
         }
     }
 
@@ -414,7 +471,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
 
 template <int BN, int STAGES, int EPI>
 cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
-    using S = Smem<BN, STAGES>;
+    using S = Smem<BN, STAGES, EPI>;
     constexpr int EW = epi_warps(EPI);
     auto kern = gemm_tc_kernel<BN, STAGES, EPI, EW>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), S::total);
@@ -483,6 +540,15 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     a.ld_pre_r = g.ld_pre_r;
     a.ld_pre_s = g.ld_pre_s;
     a.status = status;
+    if (EPI == 0) {   // box-store maps of the outputs (the slot of an absent group copies the other)
+        const bool r_ok = g.n_routed > 0 &&
+                          encode_out_map(&a.o_r, g.out_r, g.a_rows_r, (uint64_t)g.n_cols_r, g.ld_r);
+        const bool s_ok = shared &&
+                          encode_out_map(&a.o_s, g.out_s, g.T_shared, (uint64_t)g.n_cols_s, g.ld_s);
+        if ((g.n_routed > 0 && !r_ok) || (shared && !s_ok)) return cudaErrorInvalidValue;
+        if (!r_ok) a.o_r = a.o_s;
+        if (!s_ok) a.o_s = a.o_r;
+    }
     // upper bound of the tiles: sum over groups of ceil(M_j / 128) <= rows/128 + groups
     const long routed_mblk = g.n_routed > 0 ? (long)(g.max_routed_rows / BM) + g.n_routed : 0;
     const long max_tiles = routed_mblk * a.gt.n_tiles_r +

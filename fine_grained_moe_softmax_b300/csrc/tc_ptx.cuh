@@ -62,6 +62,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 2D tiled store of a shared-memory box to global memory at (x, y), tracked by the issuing
+// thread's bulk async-groups. Box elements outside the tensor's extents are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::
+                     "l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 3D tiled store of a shared-memory box to global memory at (x, y, z), tracked by the issuing
 // thread's bulk async-groups. Box elements outside the tensor's extents are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
