@@ -155,6 +155,10 @@ template <int BN, int STAGES, int EPI, int EW>
 __global__ void __launch_bounds__((2 + EW) * 32, 1)
     gemm_tc_kernel(const __grid_constant__ TcArgs args) {
     static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
+    static_assert(BN % 32 == 0 && BN >= 128 && BN <= 256 && (BN / 32) % (EW / 4) == 0,
+                  "tile width: the MMA's N (a multiple of 16 up to 256), whole 32-column chunks");
+    // two accumulators of BN columns; allocations are powers of two
+    constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256u : 512u;
     using S = Smem<BN, STAGES, EPI>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), 2 * BN);
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), kTmemCols);
         ptx::tmem_relinquish();
     }
     pdl_wait();
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, 2 * BN);
+        ptx::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -483,23 +487,35 @@ cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-// 256-column tiles unless they would waste more than a tenth of the computed columns.
-int pick_bn(int n_r, int n_s) {
-    long pad256 = 0, pad128 = 0, cols = 0;
-    for (int n : {n_r, n_s}) {
-        if (n <= 0) continue;
-        cols += n;
-        pad256 += (n + 255) / 256 * 256;
-        pad128 += (n + 127) / 128 * 128;
+// Tile width: the widest of 256 / 192 / 160 / 128 columns whose padding is at most a tenth of
+// the computed columns, else the one with the least padding. Wider tiles read less operand data
+// from L2 per FLOP; the 8-warp SwiGLU-backward epilogue needs a multiple of 64.
+int pick_bn(int n_r, int n_s, int epi) {
+    const int cands[4] = {256, 192, 160, 128};
+    int best = 128;
+    long best_pad = -1;
+    for (int bn : cands) {
+        if (epi == 2 && bn % 64 != 0) continue;
+        long padded = 0, cols = 0;
+        for (int n : {n_r, n_s}) {
+            if (n <= 0) continue;
+            cols += n;
+            padded += (long)(n + bn - 1) / bn * bn;
+        }
+        if (cols == 0) return 256;
+        if ((padded - cols) * 10 <= padded) return bn;
+        if (best_pad < 0 || padded - cols < best_pad) {
+            best = bn;
+            best_pad = padded - cols;
+        }
     }
-    if (cols == 0) return 256;
-    return (pad256 - cols) * 10 <= pad256 || pad256 <= pad128 ? 256 : 128;
+    return best;
 }
 
 template <int EPI>
 cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     const bool shared = g.has_shared;
-    const int bn = pick_bn(g.n_routed > 0 ? g.n_cols_r : 0, shared ? g.n_cols_s : 0);
+    const int bn = pick_bn(g.n_routed > 0 ? g.n_cols_r : 0, shared ? g.n_cols_s : 0, EPI);
     TcArgs a{};
     if (g.n_routed > 0) {
         if (!encode_bf16_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, BM) ||
@@ -555,6 +571,10 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
                            (long)((g.T_shared + BM - 1) / BM) * a.gt.n_tiles_s;
     const int mt = (int)std::min<long>(max_tiles, 1 << 30);
     if (bn == 256) return launch_tc<256, 4, EPI>(a, mt, st);
+    if (bn == 192) return launch_tc<192, 5, EPI>(a, mt, st);
+    if constexpr (EPI != 2) {
+        if (bn == 160) return launch_tc<160, 5, EPI>(a, mt, st);
+    }
     return launch_tc<128, 6, EPI>(a, mt, st);
 }
 

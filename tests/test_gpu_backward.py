@@ -64,6 +64,7 @@ def _compare(got, want, keys=("du", "d_centroids", "d_bias", "dw_gate", "dw_up",
     dict(d=256, inter=64, T=300),
     dict(inter=16, T=77, seed=23),          # half-chunk outputs everywhere
     dict(inter=80, n_shared=3, seed=24),    # I % 32 == 16 with several shared experts
+    dict(d=384, inter=192, T=150, seed=25),  # 192-column tiles (forward, dgrad, SwiGLU bwd)
 ])
 def test_backward_matches_oracle(kw):
     got, want = _run(_shape(**kw))
@@ -96,3 +97,44 @@ def test_backward_zero_tokens():
     torch.cuda.synchronize()
     for k in ("d_centroids", "d_bias", "dw_gate", "dw_up", "dw_down"):
         assert torch.count_nonzero(g[k]) == 0
+
+
+def test_backward_full_size_sampled_du():
+    """The benchmark's 16B-like shape at its full T = 16384, in the launch configuration
+    `bench.py --backward` times: du on a seeded sample of tokens against the oracle.
+
+    du_t depends on the rest of the batch only through the selection counts, which the gradient
+    holds fixed, and through 1/T: the balance-loss part of the affinity gradient is
+    (a1 f_j + a2 f'_g) / T with f proportional to count / T. So the oracle runs on the sample with
+    the full batch's counts twice, with dh and with dh = 0. Its balance part, computed with the
+    sample's T_s, is then rescaled by (T_s / T)^2."""
+    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer, moe_device_status
+    shape = moe_inputs.CONFIGS["16b_bf16"]
+    inputs = moe_inputs.make_inputs(shape)
+    T = shape.T
+    g = torch.Generator().manual_seed(shape.seed + 5)
+    dh = torch.randn(T, shape.d, generator=g).to(torch.bfloat16)
+    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
+                     inputs["w_up"], inputs["w_down"], inputs["bias"], backward=True)
+    got = layer.backward(inputs["u"].to("cuda"), dh.to("cuda"))
+    torch.cuda.synchronize()
+    assert moe_device_status(layer.ws_bwd) == 0
+    du_gpu = to_np(got["du"])
+    del got, layer
+    torch.cuda.empty_cache()
+
+    cfg = OracleCfg.from_shape(shape)
+    r = oracle.route(cfg, inputs["u"], inputs["centroids"], inputs["bias"])
+    ok = np.nonzero(r["margin"] >= NEAR_TIE)[0]
+    rng = np.random.default_rng(11)
+    sample = np.unique(np.concatenate([ok[:2], ok[-2:], rng.choice(ok, 20, replace=False)]))
+    Ts = len(sample)
+    sub = dict(inputs)
+    sub["u"] = inputs["u"][torch.as_tensor(sample)]
+    cfg_s = OracleCfg.from_shape(shape, T=Ts)
+    dh_s = dh[torch.as_tensor(sample)].to(torch.float64).numpy()
+    w1 = oracle.backward(cfg_s, sub, dh_s, r["counts"])
+    w0 = oracle.backward(cfg_s, sub, np.zeros_like(dh_s), r["counts"])
+    du_want = w1["du"] - (1.0 - (Ts / T) ** 2) * w0["du"]
+    err = rel_l2(du_gpu[sample], du_want)
+    assert err <= TOL, f"rel-L2(du) on {Ts} sampled tokens = {err}"

@@ -87,6 +87,8 @@ def _custom(**kw):
     dict(top_k=1),                                  # top-1
     dict(T=1), dict(T=127), dict(T=128), dict(T=129),
     dict(d=64, inter=16),                           # smallest supported widths
+    dict(d=384, inter=192, T=300),                  # 192-column tiles in both GEMMs
+    dict(d=128, inter=320, T=200),                  # 160-column gate/up tiles
     dict(n_routed=256, top_k=8, n_groups=8, T=300), # widest router
     dict(dtype="f32", renormalize=1, n_shared=2),
     dict(dtype="f32", top_k=16, n_routed=16, T=77),

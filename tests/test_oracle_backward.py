@@ -99,3 +99,30 @@ def test_backward_is_affine_in_dh(oracle_lib):
     for k in ("dw_gate", "dw_up", "dw_down"):
         assert np.all(g0[k] == 0)
     assert np.abs(g0["d_centroids"]).max() > 0
+
+
+def test_du_of_a_token_needs_only_counts_and_T(oracle_lib):
+    """du_t depends on the other tokens only through the selection counts (held fixed) and the
+    1/T of the balance statistics. The balance part of the affinity gradient,
+    (a1 f_j + a2 f'_g) / T with f proportional to count / T, scales as 1 / T^2. The rows of a
+    batch's du are recovered from a sub-batch run with the batch's counts, once with dh and
+    once with dh = 0, by rescaling the latter by (T_s / T)^2. The full-size GPU check of the
+    backward rests on this."""
+    rng = np.random.default_rng(9)
+    T, d, Ks, N, I, K = 12, 8, 1, 6, 4, 2
+    inp = _inputs(rng, T, d, Ks, N, I)
+    cfg = OracleCfg(T=T, d=d, n_shared=Ks, n_routed=N, inter=I, top_k=K, n_groups=3,
+                    alpha1=0.3, alpha2=0.6)
+    dh = rng.standard_normal((T, d))
+    counts = oracle.route(cfg, inp["u"], inp["centroids"], inp["bias"])["counts"]
+    full = oracle.backward(cfg, inp, dh, counts)
+    sample = np.array([0, 4, 11])
+    sub = dict(inp)
+    sub["u"] = inp["u"][sample]
+    cs = OracleCfg(T=len(sample), d=d, n_shared=Ks, n_routed=N, inter=I, top_k=K, n_groups=3,
+                   alpha1=0.3, alpha2=0.6)
+    w1 = oracle.backward(cs, sub, dh[sample], counts)
+    w0 = oracle.backward(cs, sub, np.zeros((len(sample), d)), counts)
+    want = w1["du"] - (1.0 - (len(sample) / T) ** 2) * w0["du"]
+    np.testing.assert_allclose(want, full["du"][sample], rtol=1e-10, atol=1e-12)
+    assert np.abs(w0["du"]).max() > 0   # the balance part is present and rescaled
