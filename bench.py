@@ -399,7 +399,8 @@ def backward_flops_per_token(sh) -> float:
 
 
 def run_backward(args, sh):
-    """Times moe_layer_backward (gradients of sum dh.h + the balance losses); one JSON line."""
+    """Times moe_layer_backward (gradients of sum dh.h + the balance losses), or with --train a
+    training step: moe_layer_forward_train then moe_layer_backward_saved; one JSON line."""
     import torch
 
     import fine_grained_moe_softmax_b300 as moe
@@ -414,8 +415,17 @@ def run_backward(args, sh):
     dh = torch.randn(sh.T, sh.d, generator=g).to(torch.bfloat16).to(dev)
     del inputs
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    train = bool(getattr(args, "train", False))
+
+    def step():
+        if train:
+            layer.forward_train(u)
+            layer.backward_saved(u, dh)
+        else:
+            layer.backward(u, dh)
+
     for _ in range(args.warmup):
-        layer.backward(u, dh)
+        step()
     torch.cuda.synchronize(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -427,7 +437,7 @@ def run_backward(args, sh):
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         starts[i].record(stream)
-        layer.backward(u, dh)
+        step()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     launches = moe.moe_launch_count() - n0
@@ -436,15 +446,23 @@ def run_backward(args, sh):
         raise RuntimeError("device status after the backward")
     total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
     _, bf16_tf, _, peak_src = load_peaks()
-    tflops = backward_flops_per_token(sh) * sh.T / (total_ms / args.steps / 1e3) / 1e12
+    # a training step executes the forward (router, gate/up, down of routed and shared rows) and
+    # the gradients; the recomputing backward executes the same minus the shared down GEMM
+    fpt = backward_flops_per_token(sh) + (2.0 * sh.d * sh.inter * sh.n_shared if train else 0.0)
+    tflops = fpt * sh.T / (total_ms / args.steps / 1e3) / 1e12
+    metric = ("MoE-layer training step tokens/s (forward keeping its state, then all gradients)"
+              if train else
+              "MoE-layer backward tokens/s (gradients of u, centroids, bias, all experts)")
+    note = ("moe_layer_forward_train + moe_layer_backward_saved per step" if train else
+            "one call recomputes the forward it needs")
     print(json.dumps({
-        "metric": "MoE-layer backward tokens/s (gradients of u, centroids, bias, all experts)",
+        "metric": metric,
         "value": sh.T * args.steps / (total_ms / 1e3), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "dtype": sh.dtype, "data": "synthetic",
         "config": {"workload": sh.name, "T": sh.T, "d": sh.d, "n_shared": sh.n_shared,
                    "n_routed": sh.n_routed, "inter": sh.inter, "top_k": sh.top_k,
-                   "note": "one call recomputes the forward it needs"},
+                   "note": note},
         "executed_tflops": tflops, "frac_of_bf16_peak": tflops / bf16_tf,
         "peak_source": f"{peak_src} bf16 burst", "gpu_launches": launches, "clocks": clk}),
         flush=True)
@@ -460,6 +478,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=4096)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--train", action="store_true",
+                    help="time a training step: forward keeping its state, then the gradients")
     ap.add_argument("--backward", action="store_true",
                     help="time the layer backward instead of the forward (1 GPU)")
     ap.add_argument("--graph", action="store_true",
@@ -485,7 +505,7 @@ def main():
             torch.cuda.set_device(local_rank)
         dist.init_process_group(backend)
     try:
-        if args.backward:
+        if args.backward or args.train:
             run_backward(args, sh)
         elif args.impl == "reference":
             run_reference(args, sh, rank, world)

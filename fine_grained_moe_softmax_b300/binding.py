@@ -66,6 +66,10 @@ _SIG = {
     "moe_pack_weights_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
     "moe_layer_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                           _P, ctypes.c_size_t, _P]),
+    "moe_layer_forward_train": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                               _P, ctypes.c_size_t, _P]),
+    "moe_layer_backward_saved": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                _P, ctypes.c_size_t, _P]),
     "moe_device_status": (ctypes.c_int, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_selftest_bounded_wait": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint64, _P]),
@@ -200,6 +204,25 @@ def moe_layer_backward(cfg, u, centroids, logit_bias, packed_w, packed_bwd, dh, 
                                     _ptr(d_centroids), _ptr(d_bias), _ptr(dw_gate), _ptr(dw_up),
                                     _ptr(dw_down), _ptr(ws), _nbytes(ws), _stream(stream)),
            "moe_layer_backward")
+
+
+def moe_layer_forward_train(cfg, u, centroids, logit_bias, packed_w, h, topk_idx, topk_gate,
+                            counts, f, P, losses, ws, stream=None):
+    _check(lib().moe_layer_forward_train(ctypes.byref(cfg), _ptr(u), _ptr(centroids),
+                                         _ptr(logit_bias), _ptr(packed_w), _ptr(h), _ptr(topk_idx),
+                                         _ptr(topk_gate), _ptr(counts), _ptr(f), _ptr(P),
+                                         _ptr(losses), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "moe_layer_forward_train")
+
+
+def moe_layer_backward_saved(cfg, u, centroids, logit_bias, packed_bwd, dh, du, d_centroids,
+                             d_bias, dw_gate, dw_up, dw_down, ws, stream=None):
+    _check(lib().moe_layer_backward_saved(ctypes.byref(cfg), _ptr(u), _ptr(centroids),
+                                          _ptr(logit_bias), _ptr(packed_bwd), _ptr(dh), _ptr(du),
+                                          _ptr(d_centroids), _ptr(d_bias), _ptr(dw_gate),
+                                          _ptr(dw_up), _ptr(dw_down), _ptr(ws), _nbytes(ws),
+                                          _stream(stream)),
+           "moe_layer_backward_saved")
 
 
 def moe_device_status(ws, stream=None) -> int:

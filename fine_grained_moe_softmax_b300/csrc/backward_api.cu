@@ -39,52 +39,48 @@ template <typename T> T* at(void* ws, size_t off) {
 
 using namespace moe;
 
-extern "C" {
+namespace moe {
+namespace {
 
-size_t moe_backward_workspace_bytes(const moe_config* cfg) {
-    Dims m;
-    if (check_bwd(cfg, &m) != MOE_OK) return 0;
-    return bwd_layout(m).total;
-}
-
-size_t moe_packed_backward_bytes(const moe_config* cfg) {
-    Dims m;
-    if (check_bwd(cfg, &m) != MOE_OK) return 0;
-    return pack_bwd_layout(m).total * 2;
-}
-
-int moe_pack_weights_backward(const moe_config* cfg, const void* w_gate, const void* w_up,
-                              const void* w_down, void* packed_bwd, moe_stream_t stream) {
+// mode 0: recompute the forward state, then the gradients (moe_layer_backward); mode 1: the
+// forward state plus the shared experts' outputs, the combine and the balance statistics, leaving
+// the state in ws (moe_layer_forward_train); mode 2: the gradients from the state a mode-1 call
+// left in ws (moe_layer_backward_saved).
+int layer_train(int mode, const moe_config* cfg, const void* u, const void* centroids,
+                const float* logit_bias, const void* packed_w, const void* packed_bwd,
+                const void* dh, void* h, int32_t* topk_idx_out, float* topk_gate_out,
+                int32_t* counts_out, float* f, float* P, float* losses, float* du,
+                float* d_centroids, float* d_bias, float* dw_gate, float* dw_up, float* dw_down,
+                void* ws, size_t ws_bytes, cudaStream_t st) {
     Dims m;
     int rc = check_bwd(cfg, &m);
     if (rc != MOE_OK) return rc;
-    if (!w_gate || !w_up || !w_down || !packed_bwd || !a16(packed_bwd)) return MOE_ERR_INVALID_ARG;
-    return launch_pack_bwd(m, w_gate, w_up, w_down, packed_bwd, (cudaStream_t)stream) ==
-                   cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
-int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroids,
-                       const float* logit_bias, const void* packed_w, const void* packed_bwd,
-                       const void* dh, float* du, float* d_centroids, float* d_bias,
-                       float* dw_gate, float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
-                       moe_stream_t stream) {
-    Dims m;
-    int rc = check_bwd(cfg, &m);
-    if (rc != MOE_OK) return rc;
-    if (!centroids || !a16(centroids) || !packed_w || !a16(packed_w) || !packed_bwd ||
-        !a16(packed_bwd) || !d_centroids || !d_bias || !dw_gate || !dw_up || !dw_down ||
-        !a16(dw_gate) || !a16(dw_up) || !a16(dw_down) || !a16(d_centroids) ||
-        (m.T > 0 && (!u || !a16(u) || !dh || !a16(dh) || !du || !a16(du))))
+    const bool fwd = mode != 2, grads = mode != 1;
+    if (!centroids || !a16(centroids) || (m.T > 0 && (!u || !a16(u))))
+        return MOE_ERR_INVALID_ARG;
+    if (fwd && (!packed_w || !a16(packed_w))) return MOE_ERR_INVALID_ARG;
+    if (mode == 1 && ((m.T > 0 && (!h || !a16(h))) || !f || !P || !losses))
+        return MOE_ERR_INVALID_ARG;
+    if (grads && (!packed_bwd || !a16(packed_bwd) || !d_centroids || !d_bias || !dw_gate ||
+                  !dw_up || !dw_down || !a16(dw_gate) || !a16(dw_up) || !a16(dw_down) ||
+                  !a16(d_centroids) || (m.T > 0 && (!dh || !a16(dh) || !du || !a16(du)))))
         return MOE_ERR_INVALID_ARG;
     const BwdLayout L = bwd_layout(m);
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < L.total)
         return MOE_ERR_WORKSPACE;
-    cudaStream_t st = (cudaStream_t)stream;
     const size_t E = (size_t)m.Ks + m.N, Id = (size_t)m.I * m.d;
     int* status = at<int>(ws, L.status);
     // the status word and the tile counters of the three weight-gradient launches
     if (cudaMemsetAsync(status, 0, 4 * sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
-    if (m.T == 0 || !m.shared_active()) {
+    if (mode == 1 && m.T == 0) {   // no token: zero statistics, nothing else to produce
+        if (cudaMemsetAsync(f, 0, (size_t)m.N * 4, st) != cudaSuccess ||
+            cudaMemsetAsync(P, 0, (size_t)m.N * 4, st) != cudaSuccess ||
+            cudaMemsetAsync(losses, 0, 2 * 4, st) != cudaSuccess ||
+            (counts_out && cudaMemsetAsync(counts_out, 0, (size_t)m.N * 4, st) != cudaSuccess))
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (grads && (m.T == 0 || !m.shared_active())) {
         // no token gives a gradient to the disabled (or any, when T = 0) experts
         const size_t n_zero = m.T == 0 ? E : (size_t)m.Ks;
         if (cudaMemsetAsync(dw_gate, 0, n_zero * Id * 4, st) != cudaSuccess ||
@@ -98,7 +94,7 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
-    const PackLayout P = pack_layout(m);
+    const PackLayout PL = pack_layout(m);
     const PackBwdLayout Q = pack_bwd_layout(m);
     const char* pw = static_cast<const char*>(packed_w);
     const char* pb = static_cast<const char*>(packed_bwd);
@@ -117,11 +113,20 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
     void* d_gu_r = at<void>(ws, L.d_gu_r);
     void* d_gu_s = at<void>(ws, L.d_gu_s);
 
-    // ---- forward recompute, routed rows in padded per-expert segments ----
-    cudaError_t e = launch_router(m, u, centroids, logit_bias, topk_idx, gate,
-                                  at<int>(ws, L.tile_counts), at<float>(ws, L.tile_psum), status,
-                                  st);
-    if (e == cudaSuccess) {
+    GroupedGemm g{};
+    g.n_routed = m.N;
+    g.has_shared = shared;
+    g.T_shared = m.T;
+    g.offsets = poff;
+    g.counts = counts;
+    g.max_routed_rows = (long)R;
+
+    // ---- forward state, routed rows in padded per-expert segments ----
+    cudaError_t e = cudaSuccess;
+    if (fwd)
+        e = launch_router(m, u, centroids, logit_bias, topk_idx, gate, at<int>(ws, L.tile_counts),
+                          at<float>(ws, L.tile_psum), status, st);
+    if (fwd && e == cudaSuccess) {
         FinalizeArgs fa{};
         fa.m = m;
         fa.n_tiles = L.n_tiles;
@@ -133,27 +138,27 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
         fa.tile_base = at<int>(ws, L.tile_base);
         fa.status = status;
         fa.pad = 64;
+        if (mode == 1) {   // the balance statistics of this batch
+            fa.f_out = f;
+            fa.P_out = P;
+            fa.losses = losses;
+        }
         e = launch_route_finalize(fa, st);
     }
-    if (e == cudaSuccess)
+    if (fwd && e == cudaSuccess)
         e = launch_perm_scatter(m, topk_idx, poff, at<int>(ws, L.tile_base),
                                 at<int>(ws, L.perm_token), perm_slot, st);
-    if (e == cudaSuccess) e = launch_gather(m, u, perm_slot, x_perm, status, st, (long)R);
-    if (e == cudaSuccess) e = launch_zero_pad_rows(m, poff, counts, x_perm, d_y, (int)d, st);
-    if (e == cudaSuccess) e = launch_zero_pad_rows(m, poff, counts, act_r, nullptr, (int)I, st);
-    GroupedGemm g{};
-    g.n_routed = m.N;
-    g.has_shared = shared;
-    g.T_shared = m.T;
-    g.offsets = poff;
-    g.counts = counts;
-    g.max_routed_rows = (long)R;
-    if (e == cudaSuccess) {   // gate/up with the SwiGLU epilogue, keeping the raw values
+    if (fwd && e == cudaSuccess) e = launch_gather(m, u, perm_slot, x_perm, status, st, (long)R);
+    if (fwd && e == cudaSuccess)
+        e = launch_zero_pad_rows(m, poff, counts, x_perm, d_y, (int)d, st);
+    if (fwd && e == cudaSuccess)
+        e = launch_zero_pad_rows(m, poff, counts, act_r, nullptr, (int)I, st);
+    if (fwd && e == cudaSuccess) {   // gate/up with the SwiGLU epilogue, keeping the raw values
         GroupedGemm gu = g;
         gu.a_r = x_perm;
         gu.a_s = u;
-        gu.b_r = pw + P.gu_r * 2;
-        gu.b_s = pw + P.gu_s * 2;
+        gu.b_r = pw + PL.gu_r * 2;
+        gu.b_s = pw + PL.gu_s * 2;
         gu.a_rows_r = R;
         gu.a_rows_s = T;
         gu.k_r = gu.k_s = d;
@@ -168,23 +173,43 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
         gu.ld_s = (int)KsI;
         gu.pre_r = at<void>(ws, L.pre_r);
         gu.pre_s = at<void>(ws, L.pre_s);
-        gu.ld_pre_r = (int)(2 * I);
-        gu.ld_pre_s = (int)(2 * KsI);
+        gu.pre_rows_r = (int)R;
+        gu.pre_rows_s = (int)T;
         e = run_grouped_gemm(gu, 1, status, st);
     }
-    if (e == cudaSuccess) {   // routed expert outputs (for the gate gradients)
+    if (fwd && e == cudaSuccess) {   // routed expert outputs (also for the gate gradients)
         GroupedGemm dn = g;
-        dn.has_shared = 0;
+        dn.has_shared = mode == 1 && shared;   // the shared experts only for the layer output
         dn.a_r = act_r;
-        dn.b_r = pw + P.dn_r * 2;
+        dn.a_s = act_s;
+        dn.b_r = pw + PL.dn_r * 2;
+        dn.b_s = pw + PL.dn_s * 2;
         dn.a_rows_r = R;
+        dn.a_rows_s = T;
         dn.k_r = I;
+        dn.k_s = KsI;
         dn.b_rows_r = (uint64_t)m.N * d;
+        dn.b_rows_s = d;
         dn.b_rows_per_expert = (int)d;
-        dn.n_cols_r = (int)d;
+        dn.n_cols_r = dn.n_cols_s = (int)d;
         dn.out_r = at<void>(ws, L.y_r);
-        dn.ld_r = (int)d;
+        dn.out_s = at<void>(ws, L.y_s);
+        dn.ld_r = dn.ld_s = (int)d;
         e = run_grouped_gemm(dn, 0, status, st);
+    }
+    if (mode == 1) {   // h = u + shared outputs + gated routed outputs, and the routing outputs
+        if (e == cudaSuccess)
+            e = launch_combine(m, u, at<void>(ws, L.y_r), at<void>(ws, L.y_s), perm_slot, gate, h,
+                               status, st, (long)R);
+        const size_t tk = (size_t)m.T * m.K;
+        if (e == cudaSuccess && topk_idx_out)
+            e = cudaMemcpyAsync(topk_idx_out, topk_idx, tk * 4, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && topk_gate_out)
+            e = cudaMemcpyAsync(topk_gate_out, gate, tk * 4, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && counts_out)
+            e = cudaMemcpyAsync(counts_out, counts, (size_t)m.N * 4, cudaMemcpyDeviceToDevice,
+                                st);
+        return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     }
 
     // ---- backward ----
@@ -248,8 +273,8 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
         dd.ld_s = (int)(2 * KsI);
         dd.pre_r = at<void>(ws, L.pre_r);
         dd.pre_s = at<void>(ws, L.pre_s);
-        dd.ld_pre_r = (int)(2 * I);
-        dd.ld_pre_s = (int)(2 * KsI);
+        dd.pre_rows_r = (int)R;
+        dd.pre_rows_s = (int)T;
         e = run_grouped_gemm(dd, 2, status, st);
     }
     if (e == cudaSuccess)   // rows past each expert's count carry no gradient
@@ -324,6 +349,63 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
         e = launch_du_final(m, dh, at<void>(ws, L.d_x_s), at<void>(ws, L.d_u_r),
                             at<void>(ws, L.d_x_r), perm_slot, du, st);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+size_t moe_backward_workspace_bytes(const moe_config* cfg) {
+    Dims m;
+    if (check_bwd(cfg, &m) != MOE_OK) return 0;
+    return bwd_layout(m).total;
+}
+
+size_t moe_packed_backward_bytes(const moe_config* cfg) {
+    Dims m;
+    if (check_bwd(cfg, &m) != MOE_OK) return 0;
+    return pack_bwd_layout(m).total * 2;
+}
+
+int moe_pack_weights_backward(const moe_config* cfg, const void* w_gate, const void* w_up,
+                              const void* w_down, void* packed_bwd, moe_stream_t stream) {
+    Dims m;
+    int rc = check_bwd(cfg, &m);
+    if (rc != MOE_OK) return rc;
+    if (!w_gate || !w_up || !w_down || !packed_bwd || !a16(packed_bwd)) return MOE_ERR_INVALID_ARG;
+    return launch_pack_bwd(m, w_gate, w_up, w_down, packed_bwd, (cudaStream_t)stream) ==
+                   cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroids,
+                       const float* logit_bias, const void* packed_w, const void* packed_bwd,
+                       const void* dh, float* du, float* d_centroids, float* d_bias,
+                       float* dw_gate, float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+    return layer_train(0, cfg, u, centroids, logit_bias, packed_w, packed_bwd, dh, nullptr,
+                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, du, d_centroids,
+                       d_bias, dw_gate, dw_up, dw_down, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int moe_layer_forward_train(const moe_config* cfg, const void* u, const void* centroids,
+                            const float* logit_bias, const void* packed_w, void* h,
+                            int32_t* topk_idx, float* topk_gate, int32_t* counts, float* f,
+                            float* P, float* losses, void* ws, size_t ws_bytes,
+                            moe_stream_t stream) {
+    return layer_train(1, cfg, u, centroids, logit_bias, packed_w, nullptr, nullptr, h, topk_idx,
+                       topk_gate, counts, f, P, losses, nullptr, nullptr, nullptr, nullptr,
+                       nullptr, nullptr, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int moe_layer_backward_saved(const moe_config* cfg, const void* u, const void* centroids,
+                             const float* logit_bias, const void* packed_bwd, const void* dh,
+                             float* du, float* d_centroids, float* d_bias, float* dw_gate,
+                             float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+    return layer_train(2, cfg, u, centroids, logit_bias, nullptr, packed_bwd, dh, nullptr,
+                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, du, d_centroids,
+                       d_bias, dw_gate, dw_up, dw_down, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 }  // extern "C"

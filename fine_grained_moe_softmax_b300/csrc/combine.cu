@@ -56,12 +56,13 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims m, const E* __restric
                                                       const E* __restrict__ y_s,
                                                       const int* __restrict__ perm_slot,
                                                       const float* __restrict__ gate,
-                                                      E* __restrict__ h, int* status) {
+                                                      E* __restrict__ h, int* status,
+                                                      long row_limit) {
     constexpr int VN = Vec<E>::n;
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x;
-    const long TK = (long)m.T * m.K;
+    const long TK = row_limit;   // rows of y_r
     int rows[KMAX];
     float g[KMAX];
     bool use[KMAX];
@@ -152,27 +153,28 @@ __global__ void balance_kernel(Dims m, const int* __restrict__ counts,
 
 template <typename E, int KMAX>
 void combine_t(const Dims& m, const void* u, const void* y_r, const void* y_s, const int* perm_slot,
-               const float* gate, void* h, int* status, cudaStream_t st) {
+               const float* gate, void* h, int* status, cudaStream_t st, long row_limit) {
     const int vecs = m.d * (int)sizeof(E) / 16;                 // 16-byte vectors per row
     const int threads = vecs >= 256 ? 256 : ((vecs + 31) / 32) * 32;
     launch_pdl(combine_kernel<E, KMAX>, dim3(m.T), dim3(threads), 0, st, m,
                static_cast<const E*>(u), static_cast<const E*>(y_r), static_cast<const E*>(y_s),
-               perm_slot, gate, static_cast<E*>(h), status);
+               perm_slot, gate, static_cast<E*>(h), status, row_limit);
 }
 
 cudaError_t launch_combine(const Dims& m, const void* u, const void* y_r, const void* y_s,
                            const int* perm_slot, const float* gate, void* h, int* status,
-                           cudaStream_t st) {
+                           cudaStream_t st, long row_limit) {
     if (m.T == 0) return cudaSuccess;
+    if (row_limit <= 0) row_limit = (long)m.T * m.K;
     if (m.dtype == MOE_DTYPE_F32) {
-        if (m.K <= 4) combine_t<float, 4>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
-        else if (m.K <= 8) combine_t<float, 8>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
-        else combine_t<float, 16>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
+        if (m.K <= 4) combine_t<float, 4>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
+        else if (m.K <= 8) combine_t<float, 8>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
+        else combine_t<float, 16>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
     } else {
         using B = __nv_bfloat16;
-        if (m.K <= 4) combine_t<B, 4>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
-        else if (m.K <= 8) combine_t<B, 8>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
-        else combine_t<B, 16>(m, u, y_r, y_s, perm_slot, gate, h, status, st);
+        if (m.K <= 4) combine_t<B, 4>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
+        else if (m.K <= 8) combine_t<B, 8>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
+        else combine_t<B, 16>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
     }
     note_launches(1);
     return cudaGetLastError();

@@ -124,7 +124,7 @@ struct BwdLayout {
     size_t status, tile_counts, tile_psum, tile_base, tile_dz;
     size_t psum, poff, counts, topk_idx, gate, perm_token, perm_slot, dgate;
     size_t x_perm, pre_r, act_r, y_r, d_y, d_gu_r, d_x_r;   // [R, .] routed rows
-    size_t pre_s, act_s, d_gu_s, d_x_s;                        // [T, .] shared
+    size_t pre_s, act_s, d_gu_s, d_x_s, y_s;                   // [T, .] shared
     size_t dz, eT, d_u_r;
     size_t total;
     int n_tiles;
@@ -163,6 +163,7 @@ inline BwdLayout bwd_layout(const Dims& m) {
     L.act_s = take(T * KsI * 2);
     L.d_gu_s = take(T * 2 * KsI * 2);
     L.d_x_s = take(T * d * 2);
+    L.y_s = take(T * d * 2);   // the shared experts' output of a training forward
     L.dz = take(T * npad * 2);
     L.eT = take(d * npad * 2);
     L.d_u_r = take(T * d * 2);

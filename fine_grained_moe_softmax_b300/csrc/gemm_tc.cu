@@ -107,9 +107,9 @@ struct TcArgs {
     __nv_bfloat16* out_r;
     __nv_bfloat16* out_s;
     int ld_r, ld_s;
-    __nv_bfloat16* pre_r;         // optional (gate/up): raw accumulator values, packed columns
-    __nv_bfloat16* pre_s;
-    int ld_pre_r, ld_pre_s;
+    __nv_bfloat16* pre_r;         // optional (gate/up): raw accumulator values, packed columns,
+    __nv_bfloat16* pre_s;         // unit-major (see pre_unit)
+    int pre_rows_r, pre_rows_s;   // rows of the two buffers
     int* status;
 };
 
@@ -134,17 +134,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// The saved gate/up values (packed layout) of intermediate columns col0 .. col0+31 of one row:
-// 64 contiguous bf16, of which the second 32 exist only when col0 + 16 < n_cols.
-__device__ __forceinline__ void load_pre_chunk(uint4 (&buf)[8], const __nv_bfloat16* row, int col0,
-                                               int n_cols, bool valid) {
+// The saved raw gate/up values are stored unit-major: 16-byte unit u (packed columns 8u .. 8u+7)
+// of row r at element (u * rows + r) * 8. A warp's 32 consecutive rows then write (gate/up
+// epilogue) and read (SwiGLU-backward epilogue) 512 contiguous bytes per unit.
+__device__ __forceinline__ size_t pre_unit(int unit, int rows, int row) {
+    return ((size_t)unit * rows + row) * 8;
+}
+
+// The saved gate/up values of intermediate columns col0 .. col0+31 of one row (packed columns
+// 2 col0 .. 2 col0 + 63, units col0/4 .. col0/4 + 7), of which the second half exists only when
+// col0 + 16 < n_cols.
+__device__ __forceinline__ void load_pre_chunk(uint4 (&buf)[8], const __nv_bfloat16* pre, int rows,
+                                               int row, int col0, int n_cols, bool valid) {
     if (!valid || col0 >= n_cols) return;
-    const uint4* src = reinterpret_cast<const uint4*>(row + 2 * col0);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) buf[q] = src[q];
+    for (int q = 0; q < 4; ++q)
+        buf[q] = *reinterpret_cast<const uint4*>(pre + pre_unit(col0 / 4 + q, rows, row));
     if (col0 + 16 < n_cols) {
 #pragma unroll
-        for (int q = 4; q < 8; ++q) buf[q] = src[q];
+        for (int q = 4; q < 8; ++q)
+            buf[q] = *reinterpret_cast<const uint4*>(pre + pre_unit(col0 / 4 + q, rows, row));
     }
 }
 
@@ -336,12 +345,10 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             // before the accumulator is ready, so that their DRAM latency overlaps the main loop
             // and the previous chunk's arithmetic.
             uint4 pre_buf[2][8];
-            const __nv_bfloat16* pre_row = nullptr;
-            if constexpr (EPI == 2) {
-                pre_row = (sh ? args.pre_s : args.pre_r) +
-                          (size_t)(ti.row0 + r) * (sh ? args.ld_pre_s : args.ld_pre_r);
-                load_pre_chunk(pre_buf[0], pre_row, col_base, n_cols, valid);
-            }
+            const __nv_bfloat16* pre_in = sh ? args.pre_s : args.pre_r;
+            const int pre_rows = sh ? args.pre_rows_s : args.pre_rows_r;
+            if constexpr (EPI == 2)
+                load_pre_chunk(pre_buf[0], pre_in, pre_rows, ti.row0 + r, col_base, n_cols, valid);
             int ok = 1;
             if (lane == 0)
                 ok = wait_phase(ptx::smem_addr(&tfull[acc]), acc_phase, abort_flag, args.status);
@@ -358,7 +365,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                 ptx::tmem_ld_32x32b_x32(t_base + c * 32, v);
                 if constexpr (EPI == 2) {
                     if (c + 1 < kChunks)
-                        load_pre_chunk(pre_buf[(c + 1) & 1], pre_row, col0 + 32, n_cols, valid);
+                        load_pre_chunk(pre_buf[(c + 1) & 1], pre_in, pre_rows, ti.row0 + r,
+                                       col0 + 32, n_cols, valid);
                 }
                 ptx::tmem_ld_wait();
                 if (!valid) continue;
@@ -370,11 +378,11 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                         for (int q = 0; q < 16; ++q)
                             p[q] = pack_bf16x2(__uint_as_float(v[2 * q]),
                                                __uint_as_float(v[2 * q + 1]));
-                        uint4* pd = reinterpret_cast<uint4*>(
-                            pre + (size_t)(ti.row0 + r) * (sh ? args.ld_pre_s : args.ld_pre_r) + col0);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            pd[q] = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+                        for (int q = 0; q < 4; ++q)   // packed columns col0.. = units col0/8..
+                            *reinterpret_cast<uint4*>(
+                                pre + pre_unit(col0 / 8 + q, pre_rows, ti.row0 + r)) =
+                                make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
                     }
                     uint32_t o[8];
 #pragma unroll
@@ -553,8 +561,8 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     a.ld_s = g.ld_s;
     a.pre_r = static_cast<__nv_bfloat16*>(g.pre_r);
     a.pre_s = static_cast<__nv_bfloat16*>(g.pre_s);
-    a.ld_pre_r = g.ld_pre_r;
-    a.ld_pre_s = g.ld_pre_s;
+    a.pre_rows_r = g.pre_rows_r;
+    a.pre_rows_s = g.pre_rows_s;
     a.status = status;
     if (EPI == 0) {   // box-store maps of the outputs (the slot of an absent group copies the other)
         const bool r_ok = g.n_routed > 0 &&

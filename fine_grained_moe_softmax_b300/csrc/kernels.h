@@ -86,8 +86,8 @@ struct GroupedGemm {
     int b_rows_per_expert, n_cols_r, n_cols_s;
     void *out_r, *out_s;
     int ld_r, ld_s;
-    void *pre_r, *pre_s;
-    int ld_pre_r, ld_pre_s;
+    void *pre_r, *pre_s;          // raw gate/up values (unit-major, see gemm_tc.cu)
+    int pre_rows_r, pre_rows_s;   // their row counts
     int n_routed, has_shared, T_shared;
     const int* offsets;
     const int* counts;
@@ -135,10 +135,11 @@ cudaError_t launch_router_bwd(const Dims& m, const void* u, const void* centroid
                               const int* counts, void* dz, float* tile_dz, int* status,
                               cudaStream_t st);
 
-// h = u + y_s + sum_k gate * y_r[perm_slot].
+// h = u + y_s + sum_k gate * y_r[perm_slot]; rows of y_r outside [0, row_limit) (default
+// T*K') are reported as corrupt and skipped.
 cudaError_t launch_combine(const Dims& m, const void* u, const void* y_r, const void* y_s,
                            const int* perm_slot, const float* gate, void* h, int* status,
-                           cudaStream_t st);
+                           cudaStream_t st, long row_limit = 0);
 
 // f, P, losses from counts and psum.
 cudaError_t launch_balance(const Dims& m, const int* counts, const float* psum, float* f,

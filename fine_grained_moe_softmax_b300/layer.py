@@ -84,19 +84,47 @@ class MoELayer:
             raise RuntimeError("construct the layer with backward=True")
         T = u.shape[0]
         cfg = self.cfg_for(T)
-        c, dev = self.cfg, self.device
-        E = c.n_shared + c.n_routed
-        f32 = torch.float32
-        g = {"du": torch.empty(T, c.d, dtype=f32, device=dev),
-             "d_centroids": torch.empty(c.n_routed, c.d, dtype=f32, device=dev),
-             "d_bias": torch.empty(c.n_routed, dtype=f32, device=dev),
-             "dw_gate": torch.empty(E, c.inter, c.d, dtype=f32, device=dev),
-             "dw_up": torch.empty(E, c.inter, c.d, dtype=f32, device=dev),
-             "dw_down": torch.empty(E, c.d, c.inter, dtype=f32, device=dev)}
+        g = self._grad_buffers(T)
         B.moe_layer_backward(cfg, u, self.centroids, self.logit_bias, self.packed,
                              self.packed_bwd, dh, g["du"], g["d_centroids"], g["d_bias"],
                              g["dw_gate"], g["dw_up"], g["dw_down"], self.ws_bwd, stream)
         return g
+
+    def forward_train(self, u: torch.Tensor, h: Optional[torch.Tensor] = None, stream=None):
+        """Forward of a training step (moe_layer_forward_train): returns h like ``forward`` and
+        keeps in the backward workspace what ``backward_saved`` needs."""
+        if self.ws_bwd is None:
+            raise RuntimeError("construct the layer with backward=True")
+        T = u.shape[0]
+        cfg = self.cfg_for(T)
+        out = self.h[:T] if h is None else h
+        B.moe_layer_forward_train(cfg, u, self.centroids, self.logit_bias, self.packed, out,
+                                  self.topk_idx[:T], self.topk_gate[:T], self.counts, self.f,
+                                  self.P, self.losses, self.ws_bwd, stream)
+        self._saved_T = T
+        return out
+
+    def backward_saved(self, u: torch.Tensor, dh: torch.Tensor, stream=None) -> dict:
+        """Gradients like ``backward`` from the state of the last ``forward_train`` on the same u
+        (moe_layer_backward_saved), without recomputing the forward."""
+        T = u.shape[0]
+        if getattr(self, "_saved_T", None) != T:
+            raise RuntimeError("backward_saved needs a forward_train on the same batch first")
+        g = self._grad_buffers(T)
+        B.moe_layer_backward_saved(self.cfg_for(T), u, self.centroids, self.logit_bias,
+                                   self.packed_bwd, dh, g["du"], g["d_centroids"], g["d_bias"],
+                                   g["dw_gate"], g["dw_up"], g["dw_down"], self.ws_bwd, stream)
+        return g
+
+    def _grad_buffers(self, T: int) -> dict:
+        c, dev, f32 = self.cfg, self.device, torch.float32
+        E = c.n_shared + c.n_routed
+        return {"du": torch.empty(T, c.d, dtype=f32, device=dev),
+                "d_centroids": torch.empty(c.n_routed, c.d, dtype=f32, device=dev),
+                "d_bias": torch.empty(c.n_routed, dtype=f32, device=dev),
+                "dw_gate": torch.empty(E, c.inter, c.d, dtype=f32, device=dev),
+                "dw_up": torch.empty(E, c.inter, c.d, dtype=f32, device=dev),
+                "dw_down": torch.empty(E, c.d, c.inter, dtype=f32, device=dev)}
 
     def capture(self, u: torch.Tensor):
         """Records one forward on the fixed input buffer ``u`` into a CUDA graph and returns

@@ -172,6 +172,28 @@ int moe_layer_backward(const moe_config* cfg, const void* u, const void* centroi
                        float* dw_gate, float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
 
+/* A training step without the recompute: moe_layer_forward_train computes the layer forward
+ * ([P1] §方法细节) with the outputs of moe_layer_forward (h, routing, f, P, losses; topk_idx,
+ * topk_gate and counts may be NULL) and leaves in the backward workspace `ws` everything the
+ * gradients need. moe_layer_backward_saved then computes the gradients of moe_layer_backward from
+ * that state, skipping the router, permutation, gate/up and routed down GEMMs it would otherwise
+ * recompute.
+ *   Both calls take the same cfg (same T) and the same u, centroids and logit_bias; ws
+ *   (moe_backward_workspace_bytes(cfg) bytes, 256-byte aligned) must not be used by another call
+ *   in between. The backward's results equal moe_layer_backward's bit for bit; h equals
+ *   moe_layer_forward's.
+ *   bf16 layers only; argument and workspace errors as for moe_layer_backward. */
+int moe_layer_forward_train(const moe_config* cfg, const void* u, const void* centroids,
+                            const float* logit_bias, const void* packed_w, void* h,
+                            int32_t* topk_idx, float* topk_gate, int32_t* counts, float* f,
+                            float* P, float* losses, void* ws, size_t ws_bytes,
+                            moe_stream_t stream);
+int moe_layer_backward_saved(const moe_config* cfg, const void* u, const void* centroids,
+                             const float* logit_bias, const void* packed_bwd, const void* dh,
+                             float* du, float* d_centroids, float* d_bias, float* dw_gate,
+                             float* dw_up, float* dw_down, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
 /* Waits for `stream`, then returns the device status word of `ws` (MOE_OK or a negative
  * moe_status), or MOE_ERR_CUDA if the wait itself failed. */
 int moe_device_status(const void* ws, moe_stream_t stream);

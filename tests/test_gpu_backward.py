@@ -138,3 +138,48 @@ def test_backward_full_size_sampled_du():
     du_want = w1["du"] - (1.0 - (Ts / T) ** 2) * w0["du"]
     err = rel_l2(du_gpu[sample], du_want)
     assert err <= TOL, f"rel-L2(du) on {Ts} sampled tokens = {err}"
+
+
+@pytest.mark.parametrize("shape", [
+    _shape(),
+    _shape(n_shared=3, inter=48, T=129, renormalize=1),
+    _shape(drop_shared=1, skip_top=1),
+    moe_inputs.CONFIGS["2b_bf16"].with_(T=300),
+], ids=["base", "3shared_renorm", "ablations", "2b"])
+def test_training_pair_matches_forward_and_backward(shape):
+    """moe_layer_forward_train + moe_layer_backward_saved run the same kernels on the same rows
+    as moe_layer_forward and moe_layer_backward, so h, the routing outputs, the statistics and
+    every gradient agree bit for bit; the saved path only skips the recompute."""
+    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer, moe_device_status
+    inputs = moe_inputs.make_inputs(shape)
+    g = torch.Generator().manual_seed(shape.seed + 5)
+    dh = torch.randn(shape.T, shape.d, generator=g).to(torch.bfloat16).to("cuda")
+    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
+                     inputs["w_up"], inputs["w_down"], inputs["bias"], backward=True)
+    u = inputs["u"].to("cuda")
+    h_ref = layer.forward(u).clone()
+    ref = {k: getattr(layer, k).clone() for k in ("topk_idx", "topk_gate", "counts", "f", "P",
+                                                   "losses")}
+    g_ref = layer.backward(u, dh)
+    torch.cuda.synchronize()
+    h = layer.forward_train(u).clone()
+    got = {k: getattr(layer, k).clone() for k in ref}
+    g_saved = layer.backward_saved(u, dh)
+    torch.cuda.synchronize()
+    assert moe_device_status(layer.ws_bwd) == 0
+    assert torch.equal(h, h_ref)
+    for k in ref:
+        assert torch.equal(got[k], ref[k]), k
+    for k in g_ref:
+        assert torch.equal(g_saved[k], g_ref[k]), k
+
+
+def test_backward_saved_needs_a_training_forward():
+    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer
+    shape = _shape(T=32)
+    inputs = moe_inputs.make_inputs(shape)
+    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
+                     inputs["w_up"], inputs["w_down"], backward=True)
+    u = inputs["u"].to("cuda")
+    with pytest.raises(RuntimeError):
+        layer.backward_saved(u, torch.zeros_like(u))
