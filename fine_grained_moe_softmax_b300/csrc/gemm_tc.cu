@@ -64,17 +64,19 @@ bool encode_bf16_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t 
 }
 
 // Row-major bf16 output [rows, cols] with row stride ld (elements) as a 2D TMA map for stores,
-// box [32 rows x 32 columns], 64-byte swizzle; columns >= cols and rows >= rows are clipped.
+// box [32 rows x box_cols columns] (32: 64-byte rows, 64-byte swizzle; 16: 32-byte rows, 32-byte
+// swizzle); columns >= cols and rows >= rows are clipped.
 static bool encode_out_map(CUtensorMap* map, void* ptr, uint64_t rows, uint64_t cols,
-                           uint64_t ld) {
+                           uint64_t ld, int box_cols = 32) {
     auto fn = tensor_map_encoder();
     if (!fn || !ptr || rows == 0 || cols == 0) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {ld * 2};
-    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, 32u};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
+              box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -113,9 +115,10 @@ struct TcArgs {
     int* status;
 };
 
-// EPI 0 output staging: per epilogue warp two 2 KB boxes (32 rows x 32 bf16)
-constexpr uint32_t kOutBox = 32 * 32 * 2;
-constexpr uint32_t staging_bytes(int epi) { return epi == 0 ? 4 * 2 * kOutBox : 0; }
+// Output staging of the box-store epilogues: per epilogue warp two boxes of 32 rows x 32 bf16
+// (EPI 0) or 32 rows x 16 bf16 (EPI 1: the SwiGLU of a 32-column chunk is 16 activations)
+constexpr uint32_t out_box_bytes(int epi) { return epi == 0 ? 32 * 32 * 2 : 32 * 16 * 2; }
+constexpr uint32_t staging_bytes(int epi) { return epi == 2 ? 0 : 4 * 2 * out_box_bytes(epi); }
 
 template <int BN, int STAGES, int EPI>
 struct Smem {
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* a_ring = base;
     uint8_t* b_ring = base + STAGES * S::a_bytes;
-    uint8_t* staging = base + S::ring;   // [4 warps][2][kOutBox] (EPI 0)
+    uint8_t* staging = base + S::ring;   // [4 warps][2][out box] (EPI 0 and 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + S::ring + S::staging);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         ptx::prefetch_tmap(&args.a_s);
         ptx::prefetch_tmap(&args.b_r);
         ptx::prefetch_tmap(&args.b_s);
-        if constexpr (EPI == 0) {
+        if constexpr (EPI != 2) {
             ptx::prefetch_tmap(&args.o_r);
             ptx::prefetch_tmap(&args.o_s);
         }
@@ -324,7 +327,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         constexpr int kChunks = BN / 32 / (EW / 4);     // 32-column chunks per warp and tile
         const int quarter = warp & 3;
         const int c_first = ((warp - 2) >> 2) * kChunks;
-        uint8_t* my_stage = staging + (EPI == 0 ? (warp - 2) * 2 * kOutBox : 0);
+        constexpr uint32_t kOutBox = out_box_bytes(EPI);
+        uint8_t* my_stage = staging + (EPI != 2 ? (warp - 2) * 2 * kOutBox : 0);
         int sbuf = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             const int col_base = ti.n_blk * BN + c_first * 32;
             // all 32 rows of this warp lie inside the group: the box store cannot reach rows of
             // the next group
-            const bool box_store = EPI == 0 && ti.m_blk * BM + quarter * 32 + 32 <= ti.m_rows;
+            const bool box_store = EPI != 2 && ti.m_blk * BM + quarter * 32 + 32 <= ti.m_rows;
             // EPI 2 reads the saved gate/up values of its rows one chunk ahead, the first chunk
             // before the accumulator is ready, so that their DRAM latency overlaps the main loop
             // and the previous chunk's arithmetic.
@@ -392,9 +396,30 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                         const float u1 = __uint_as_float(v[16 + 2 * q + 1]);
                         o[q] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(out + orow + col0 / 2);
-                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    if (box_store) {   // 32 rows x 16 activations through shared memory
+                        if (lane == 0) ptx::bulk_wait_read<1>();
+                        __syncwarp();
+                        uint8_t* buf = my_stage + sbuf * kOutBox;
+                        // 32-byte rows, 32-byte swizzle: 16-byte half q of row r sits at
+                        // position q ^ ((r >> 2) & 1)
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            *reinterpret_cast<uint4*>(buf + lane * 32 +
+                                                      ((q ^ ((lane >> 2) & 1)) << 4)) =
+                                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(sh ? &args.o_s : &args.o_r, ptx::smem_addr(buf),
+                                              col0 / 2, ti.row0 + ti.m_blk * BM + quarter * 32);
+                            ptx::bulk_commit();
+                        }
+                        sbuf ^= 1;
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(out + orow + col0 / 2);
+                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
                 } else if constexpr (EPI == 2) {
                     // columns col0 .. col0+31 are intermediate indices i; their gate/up values
                     // are the packed blocks col0/16 and col0/16 + 1 (32 values each) of pre_buf
@@ -466,7 +491,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                 acc_phase ^= 1;
             }
         }
-        if constexpr (EPI == 0) {   // the box stores read shared memory until they finish
+        if constexpr (EPI != 2) {   // the box stores read shared memory until they finish
             if (lane == 0) ptx::bulk_wait_all();
         }
     }
@@ -564,11 +589,15 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     a.pre_rows_r = g.pre_rows_r;
     a.pre_rows_s = g.pre_rows_s;
     a.status = status;
-    if (EPI == 0) {   // box-store maps of the outputs (the slot of an absent group copies the other)
+    if (EPI != 2) {   // box-store maps of the outputs (the slot of an absent group copies the other)
+        // EPI 1 writes one activation per gate/up column pair: half the GEMM's columns
+        const int div = EPI == 1 ? 2 : 1, box_cols = EPI == 1 ? 16 : 32;
         const bool r_ok = g.n_routed > 0 &&
-                          encode_out_map(&a.o_r, g.out_r, g.a_rows_r, (uint64_t)g.n_cols_r, g.ld_r);
+                          encode_out_map(&a.o_r, g.out_r, g.a_rows_r, (uint64_t)(g.n_cols_r / div),
+                                         g.ld_r, box_cols);
         const bool s_ok = shared &&
-                          encode_out_map(&a.o_s, g.out_s, g.T_shared, (uint64_t)g.n_cols_s, g.ld_s);
+                          encode_out_map(&a.o_s, g.out_s, g.T_shared, (uint64_t)(g.n_cols_s / div),
+                                         g.ld_s, box_cols);
         if ((g.n_routed > 0 && !r_ok) || (shared && !s_ok)) return cudaErrorInvalidValue;
         if (!r_ok) a.o_r = a.o_s;
         if (!s_ok) a.o_s = a.o_r;
