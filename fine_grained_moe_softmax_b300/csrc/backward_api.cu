@@ -1,6 +1,8 @@
-// backward_api.cu -- C ABI of the layer backward (include/moe_b300.h): argument checks and the
-// order of launches. The backward recomputes the forward pieces it needs from the inputs, then
-// runs the chain rule stage by stage; all intermediates live in the caller's workspace.
+// backward_api.cu -- C ABI of the layer backward and of the training pair (include/moe_b300.h):
+// argument checks and the order of launches. The stateless backward recomputes the forward pieces
+// it needs from the inputs, then runs the chain rule stage by stage. The training forward
+// computes those pieces once, together with the layer output, and the saved backward starts from
+// them. All intermediates live in the caller's workspace.
 #include <algorithm>
 
 #include "common.cuh"

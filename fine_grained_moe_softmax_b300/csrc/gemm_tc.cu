@@ -8,16 +8,17 @@
 //
 // Kernel shape: persistent, one CTA per SM, 2 + EW warps.
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] (bf16, 128-byte swizzle) per
-//               stage into a STAGES-deep shared-memory ring.
-//   warp 1      allocates 2*BN TMEM columns; one thread issues tcgen05.mma (M=128, N=BN, K=16)
-//               into one of two fp32 accumulators, and commits stage releases and tile completion
-//               to mbarriers.
+//               stage into a STAGES-deep shared-memory ring; BN = 256, 192, 160 or 128 columns,
+//               the widest that pads the group widths by at most a tenth.
+//   warp 1      allocates the TMEM of two BN-column accumulators (a power of two of columns); one
+//               thread issues tcgen05.mma (M=128, N=BN, K=16) into one of them, and commits stage
+//               releases and tile completion to mbarriers.
 //   warps 2..   EW = 4 or 8 epilogue warps: tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32*(w%4)..; with 8 warps two share each lane quarter and split its columns),
-//               SwiGLU (backward) or plain conversion to bf16. The plain epilogue stages each
-//               warp's 32 rows x 32 columns in shared memory (64-byte swizzle) and writes them with
-//               a TMA bulk store; the others (and a warp whose rows cross the end of a group) store
-//               valid rows/columns directly.
+//               then SwiGLU, SwiGLU backward or plain conversion to bf16. The plain and SwiGLU
+//               epilogues stage each warp's 32 rows x 32 outputs (x 16 for SwiGLU) in shared memory
+//               (swizzled) and write them with a TMA bulk store; the SwiGLU-backward epilogue, and
+//               any warp whose rows cross the end of a group, store valid rows/columns directly.
 // Two accumulators let the epilogue of tile i overlap the main loop of tile i+1. Every wait on an
 // mbarrier is bounded in time; on expiry the kernel records MOE_ERR_TIMEOUT, stops issuing work,
 // drains what it issued and frees its TMEM before returning.
@@ -92,10 +93,7 @@ constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle r
 
 // Epilogue warps per EPI (below): 4 suffice for the forward epilogues; the SwiGLU-backward epilogue
 // loads the saved gate/up values and does twice the arithmetic, and needs 8 to keep up.
-#ifndef MOE_GEMM_FWD_EPI_WARPS
-#define MOE_GEMM_FWD_EPI_WARPS 4
-#endif
-constexpr int epi_warps(int epi) { return epi == 2 ? 8 : MOE_GEMM_FWD_EPI_WARPS; }
+constexpr int epi_warps(int epi) { return epi == 2 ? 8 : 4; }
 
 struct TcArgs {
     CUtensorMap a_r, a_s, b_r, b_s;
