@@ -118,9 +118,14 @@ struct TcArgs {
 constexpr uint32_t out_box_bytes(int epi) { return epi == 0 ? 32 * 32 * 2 : 32 * 16 * 2; }
 constexpr uint32_t staging_bytes(int epi) { return epi == 2 ? 0 : 4 * 2 * out_box_bytes(epi); }
 
-template <int BN, int STAGES, int EPI>
+// ABOX: rows of A loaded per tile. A batch of at most 64 tokens gives every group at most 64
+// rows, so its A slot holds 64 rows (8 KB) and the ring gets one more stage; the MMA still reads
+// 128 rows, the other 64 from the shared memory that follows (in bounds), and those rows' outputs
+// are never stored (an output row depends only on its own A row).
+template <int BN, int STAGES, int EPI, int ABOX = BM>
 struct Smem {
-    static constexpr uint32_t a_bytes = BM * BK * 2;
+    static_assert(ABOX == BM || ABOX == 64, "A rows per tile");
+    static constexpr uint32_t a_bytes = ABOX * BK * 2;
     static constexpr uint32_t b_bytes = BN * BK * 2;
     static constexpr uint32_t ring = STAGES * (a_bytes + b_bytes);
     static constexpr uint32_t staging = staging_bytes(EPI);
@@ -161,7 +166,7 @@ __device__ __forceinline__ void load_pre_chunk(uint4 (&buf)[8], const __nv_bfloa
 // EPI: 0 plain bf16 store; 1 SwiGLU of packed gate/up column pairs (expert FFN forward);
 // 2 SwiGLU backward: the accumulator is d_act, and with the saved gate/up values of the same rows
 // (pre, packed) the epilogue writes d_gate / d_up (packed) to out.
-template <int BN, int STAGES, int EPI, int EW>
+template <int BN, int STAGES, int EPI, int EW, int ABOX>
 __global__ void __launch_bounds__((2 + EW) * 32, 1)
     gemm_tc_kernel(const __grid_constant__ TcArgs args) {
     static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                   "tile width: the MMA's N (a multiple of 16 up to 256), whole 32-column chunks");
     // two accumulators of BN columns; allocations are powers of two
     constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256u : 512u;
-    using S = Smem<BN, STAGES, EPI>;
+    using S = Smem<BN, STAGES, EPI, ABOX>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -504,11 +509,11 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
 
 // ------------------------------------------------------------------------- host side ----
 
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, int ABOX = BM>
 cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
-    using S = Smem<BN, STAGES, EPI>;
+    using S = Smem<BN, STAGES, EPI, ABOX>;
     constexpr int EW = epi_warps(EPI);
-    auto kern = gemm_tc_kernel<BN, STAGES, EPI, EW>;
+    auto kern = gemm_tc_kernel<BN, STAGES, EPI, EW, ABOX>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), S::total);
     if (e != cudaSuccess) return e;
     const int grid = max(1, min(sm_count(), max_tiles));
@@ -547,14 +552,17 @@ template <int EPI>
 cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     const bool shared = g.has_shared;
     const int bn = pick_bn(g.n_routed > 0 ? g.n_cols_r : 0, shared ? g.n_cols_s : 0, EPI);
+    // at most 64 tokens: every group (routed or shared) has at most 64 rows
+    const bool small_a = EPI != 2 && bn == 256 && g.T_shared > 0 && g.T_shared <= 64;
+    const int a_box = small_a ? 64 : BM;
     TcArgs a{};
     if (g.n_routed > 0) {
-        if (!encode_bf16_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, BM) ||
+        if (!encode_bf16_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, a_box) ||
             !encode_bf16_map(&a.b_r, g.b_r, g.b_rows_r, g.k_r, bn))
             return cudaErrorInvalidValue;
     }
     if (shared) {
-        if (!encode_bf16_map(&a.a_s, g.a_s, g.a_rows_s, g.k_s, BM) ||
+        if (!encode_bf16_map(&a.a_s, g.a_s, g.a_rows_s, g.k_s, a_box) ||
             !encode_bf16_map(&a.b_s, g.b_s, g.b_rows_s, g.k_s, bn))
             return cudaErrorInvalidValue;
     }
@@ -605,6 +613,9 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     const long max_tiles = routed_mblk * a.gt.n_tiles_r +
                            (long)((g.T_shared + BM - 1) / BM) * a.gt.n_tiles_s;
     const int mt = (int)std::min<long>(max_tiles, 1 << 30);
+    if constexpr (EPI != 2) {
+        if (small_a) return launch_tc<256, 5, EPI, 64>(a, mt, st);
+    }
     if (bn == 256) return launch_tc<256, 4, EPI>(a, mt, st);
     if (bn == 192) return launch_tc<192, 5, EPI>(a, mt, st);
     if constexpr (EPI != 2) {

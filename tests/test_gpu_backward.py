@@ -65,6 +65,7 @@ def _compare(got, want, keys=("du", "d_centroids", "d_bias", "dw_gate", "dw_up",
     dict(inter=16, T=77, seed=23),          # half-chunk outputs everywhere
     dict(inter=80, n_shared=3, seed=24),    # I % 32 == 16 with several shared experts
     dict(d=384, inter=192, T=150, seed=25),  # 192-column tiles (forward, dgrad, SwiGLU bwd)
+    dict(d=256, inter=128, T=48, seed=26),   # <= 64 tokens: 64-row A tiles in the forward GEMMs
 ])
 def test_backward_matches_oracle(kw):
     got, want = _run(_shape(**kw))

@@ -89,6 +89,7 @@ def _custom(**kw):
     dict(d=64, inter=16),                           # smallest supported widths
     dict(d=384, inter=192, T=300),                  # 192-column tiles in both GEMMs
     dict(d=128, inter=320, T=200),                  # 160-column gate/up tiles
+    dict(d=256, inter=128, T=40),                   # <= 64 tokens: 64-row A tiles, 5 stages
     dict(n_routed=256, top_k=8, n_groups=8, T=300), # widest router
     dict(dtype="f32", renormalize=1, n_shared=2),
     dict(dtype="f32", top_k=16, n_routed=16, T=77),
