@@ -44,6 +44,17 @@ def gate_up_flops(sh, T) -> float:
     return 4.0 * sh.d * sh.inter * T * (sh.n_shared + sh.top_k)
 
 
+def workload_config(sh, T, world, graph=False) -> dict:
+    """The `config` object of a bench line; both arms describe the workload the same way."""
+    return {"workload": sh.name, "T": T, "d": sh.d, "n_shared": sh.n_shared,
+            "n_routed": sh.n_routed, "inter": sh.inter, "top_k": sh.top_k,
+            "global_batch": T * world, "parallelism": f"replicas x{world}",
+            "l2": "flushed between timed steps (512 MB write outside the events)",
+            "launch": "CUDA graph replay of moe_layer_forward" if graph
+                      else "direct moe_layer_forward calls",
+            "inputs": "seeded Gaussian tensors of the workload's shape"}
+
+
 def gate_up_bytes(sh, T, counts) -> float:
     """Algorithmic DRAM bytes of one gate/up launch: the gate and up weights of the shared
     experts and of every routed expert that received a token, the A rows it reads (T K' routed
@@ -196,8 +207,7 @@ def run_reference(args, sh, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": sh.name, "T": sh.T, "d": sh.d, "n_shared": sh.n_shared,
-                   "n_routed": sh.n_routed, "inter": sh.inter, "top_k": sh.top_k},
+        "config": workload_config(sh, sh.T, world, graph=False),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -362,13 +372,7 @@ def run_ours(args, sh, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": sh.dtype, "data": "synthetic",
-        "config": {"workload": sh.name, "T": T, "d": sh.d, "n_shared": sh.n_shared,
-                   "n_routed": sh.n_routed, "inter": sh.inter, "top_k": sh.top_k,
-                   "global_batch": T * world, "parallelism": f"replicas x{world}",
-                   "l2": "flushed between timed steps (512 MB write outside the events)",
-                   "launch": "CUDA graph replay of moe_layer_forward" if graph is not None
-                             else "direct moe_layer_forward calls",
-                   "inputs": "seeded Gaussian tensors of the workload's shape"},
+        "config": workload_config(sh, T, world, graph=graph is not None),
         "roofline": roof,
         "layer_roofline": {"achieved_tflops": layer_tflops, "frac_of_bf16_peak":
                            layer_tflops / bf16_tf, "flops_per_token": flops_per_token(sh)},

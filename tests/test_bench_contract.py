@@ -1,0 +1,61 @@
+"""The JSON line of bench.py: the keys, types and cross-arm consistency that the benchmark
+contract asks for (one line on stdout; the reference arm times the oracle and runs on CPU)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BASE_KEYS = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+             "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "e2e")
+
+
+def _bench(*args, timeout=900):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                         capture_output=True, text=True, timeout=timeout)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, out.stdout[-3000:]
+    return json.loads(lines[0])
+
+
+def _check_base(line, steps, warmup):
+    for k in BASE_KEYS:
+        assert k in line, k
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["steps"] == steps and line["warmup"] == warmup and line["n_gpus"] == 1
+    assert line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert line["config"]["workload"] and line["config"]["global_batch"] == line["config"]["T"]
+    e2e = line["e2e"]
+    assert e2e["value"] > 0 and e2e["unit"] == line["unit"]
+    assert "h2d_bytes_per_step" in e2e and "d2h_bytes_per_step" in e2e
+
+
+def test_reference_arm_line():
+    line = _bench("--impl", "reference", "--config", "tiny_f32", "--steps", "2", "--warmup", "3")
+    _check_base(line, 2, 3)
+    assert line["impl"] == "reference"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert cb["unit"] == line["unit"] and cb["sample"]
+    assert line["e2e"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.gpu
+def test_our_arm_line_matches_the_reference_arm():
+    ours = _bench("--config", "2b_bf16", "--steps", "3", "--warmup", "3", "--no-cpu-baseline")
+    _check_base(ours, 3, 3)
+    roof = ours["roofline"]
+    assert roof["bound"] in ("tensor", "hbm") and roof["unit"] in ("TFLOP/s", "GB/s")
+    assert roof["achieved"] > 0 and roof["peak"] > 0
+    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-9
+    assert "traffic" in roof
+    assert ours["gpu_launches"] > 0
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(ours["clocks"])
+    assert ours["e2e"]["h2d_bytes_per_step"] > 0 and ours["e2e"]["d2h_bytes_per_step"] > 0
+    ref = _bench("--impl", "reference", "--config", "2b_bf16", "--steps", "1", "--warmup", "3")
+    for k in ("metric", "unit", "higher_is_better", "config"):
+        assert ours[k] == ref[k], k
