@@ -173,6 +173,40 @@ inline BwdLayout bwd_layout(const Dims& m) {
 
 // ------------------------------------------------------------------------ device utils ----
 
+// Balance statistics in one fixed order shared by every kernel that produces them:
+//   f_j = N' / (K' T) count_j and P_j = psum_j / T (balance_fp, one expert at a time), then
+//   L_ExpBal = a1 sum_j f_j P_j and L_DevBal = a2 sum_g mean_{j in G_g}(f_j) * sum_{j in G_g} P_j
+//   over D contiguous groups, the first N' mod D one expert larger (balance_losses, one thread,
+//   from the f_j and P_j already computed).
+__device__ inline void balance_fp(const Dims& m, int total_j, float ptot_j, float* f_j,
+                                  float* P_j) {
+    const float Tf = (float)max(m.T, 1);
+    const float scale = (float)m.N / ((float)m.K * Tf);
+    *f_j = scale * (float)total_j;
+    *P_j = ptot_j / Tf;
+}
+
+__device__ inline void balance_losses(const Dims& m, const float* f, const float* P,
+                                      float* losses) {
+    const int N = m.N;
+    float lexp = 0.f, ldev = 0.f;
+    for (int j = 0; j < N; ++j) lexp += f[j] * P[j];
+    const int base = N / m.D, extra = N % m.D;
+    int first = 0;
+    for (int g = 0; g < m.D; ++g) {
+        const int size = base + (g < extra ? 1 : 0);
+        float fs = 0.f, ps = 0.f;
+        for (int j = first; j < first + size; ++j) {
+            fs += f[j];
+            ps += P[j];
+        }
+        ldev += (fs / (float)size) * ps;
+        first += size;
+    }
+    losses[0] = m.a1 * lexp;
+    losses[1] = m.a2 * ldev;
+}
+
 // First error wins; later errors leave the word alone.
 __device__ __forceinline__ void set_status(int* status, int code) {
     if (status) atomicCAS(status, 0, code);

@@ -17,10 +17,24 @@ cudaError_t launch_router(const Dims& m, const void* u, const void* centroids, c
                           int* topk_idx, float* topk_gate, int* tile_counts, float* tile_psum,
                           int* status, cudaStream_t st);
 
-// Tensor-core router of bf16 layers (same outputs as launch_router).
+// Outputs a one-tile batch (T <= 128) can get from the router directly, in place of
+// launch_route_finalize + launch_perm_scatter (same values; f, P, losses may be null).
+struct SingleTileTables {
+    int* counts;
+    float* psum;
+    int* offsets;
+    int* perm_token;
+    int* perm_slot;
+    float *f, *P, *losses;
+    int pad;
+};
+
+// Tensor-core router of bf16 layers (same outputs as launch_router; with `tables`, a one-tile
+// batch also gets its routing tables).
 cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids,
                              const float* bias, int* topk_idx, float* topk_gate, int* tile_counts,
-                             float* tile_psum, int* status, cudaStream_t st);
+                             float* tile_psum, int* status, cudaStream_t st,
+                             const SingleTileTables* tables = nullptr);
 
 // The driver's tensor-map encoder (resolved once through the runtime), or null.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

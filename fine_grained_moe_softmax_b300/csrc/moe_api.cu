@@ -297,10 +297,16 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
 
     if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(0);
-    cudaError_t e = launch_router(m, u, centroids, logit_bias, topk_idx, topk_gate, tc, tp, status,
-                                  st);
+    // a one-tile bf16 batch gets its routing tables from the router itself (no finalize and
+    // scatter launches)
+    const bool one_tile = m.dtype == MOE_DTYPE_BF16 && L.n_tiles == 1;
+    SingleTileTables tab{counts, psum, offsets, perm_token, perm_slot, f, P, losses, 0};
+    cudaError_t e = one_tile ? launch_router_tc(m, u, centroids, logit_bias, topk_idx, topk_gate,
+                                                tc, tp, status, st, &tab)
+                             : launch_router(m, u, centroids, logit_bias, topk_idx, topk_gate, tc,
+                                             tp, status, st);
     mk.mark(1);
-    if (e == cudaSuccess) {   // totals, offsets, tile bases and the balance statistics
+    if (e == cudaSuccess && !one_tile) {   // totals, offsets, tile bases, statistics
         FinalizeArgs fa{};
         fa.m = m;
         fa.n_tiles = L.n_tiles;
@@ -316,7 +322,7 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
         fa.status = status;
         e = launch_route_finalize(fa, st);
     }
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !one_tile)
         e = launch_perm_scatter(m, topk_idx, offsets, tb, perm_token, perm_slot, st);
     mk.mark(2);
     if (e == cudaSuccess) e = launch_gather(m, u, perm_slot, at<void>(ws, L.x_perm), status, st);

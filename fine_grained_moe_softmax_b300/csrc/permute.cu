@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(1024) route_finalize_kernel(FinalizeArgs a) {
     __shared__ int total[kMaxRouted];
     __shared__ float ptot[kMaxRouted];
     __shared__ int off[kMaxRouted + 1];
+    __shared__ float fs[kMaxRouted], Ps[kMaxRouted];
     pdl_wait();
     pdl_trigger();
     const Dims m = a.m;
@@ -97,37 +98,20 @@ __global__ void __launch_bounds__(1024) route_finalize_kernel(FinalizeArgs a) {
         }
         off[N] = acc;
     }
-    if (threadIdx.x == 32 && a.losses) {   // balance statistics, same arithmetic as balance_kernel
-        const float Tf = (float)max(m.T, 1);
-        const float scale = (float)N / ((float)m.K * Tf);
-        float lexp = 0.f, ldev = 0.f;
-        for (int j = 0; j < N; ++j) lexp += (scale * (float)total[j]) * (ptot[j] / Tf);
-        const int base = N / m.D, extra = N % m.D;
-        int first = 0;
-        for (int g = 0; g < m.D; ++g) {
-            const int size = base + (g < extra ? 1 : 0);
-            float fs = 0.f, ps = 0.f;
-            for (int j = first; j < first + size; ++j) {
-                fs += scale * (float)total[j];
-                ps += ptot[j] / Tf;
-            }
-            ldev += (fs / (float)size) * ps;
-            first += size;
-        }
-        a.losses[0] = m.a1 * lexp;
-        a.losses[1] = m.a2 * ldev;
-    }
+    __syncthreads();
+    if (a.f_out || a.losses)   // f_j and P_j, then the losses from them
+        for (int j = threadIdx.x; j < N; j += blockDim.x)
+            balance_fp(m, total[j], ptot[j], &fs[j], &Ps[j]);
+    __syncthreads();
+    if (threadIdx.x == 32 && a.losses) balance_losses(m, fs, Ps, a.losses);
     __syncthreads();
     if (a.offsets)
         for (int j = threadIdx.x; j <= N; j += blockDim.x) a.offsets[j] = off[j];
-    if (a.f_out) {
-        const float Tf = (float)max(m.T, 1);
-        const float scale = (float)N / ((float)m.K * Tf);
+    if (a.f_out)
         for (int j = threadIdx.x; j < N; j += blockDim.x) {
-            a.f_out[j] = scale * (float)total[j];
-            a.P_out[j] = ptot[j] / Tf;
+            a.f_out[j] = fs[j];
+            a.P_out[j] = Ps[j];
         }
-    }
 }
 
 // One CTA per 128-token tile. Each assignment a = t_local*K' + k sets bit a of its expert's

@@ -46,6 +46,16 @@ struct RouterArgs {
     float* tile_dz;       // [N'][n_tiles] out: per-tile sums of dz
     float a1, a2;
     int D;
+    // a batch of one tile (T <= 128) can finish its routing tables here, in place of the finalize
+    // and scatter kernels: fused != 0 and the outputs below
+    int fused, pad;
+    Dims dims;
+    int* counts_out;      // [N']
+    float* psum_out;      // [N']
+    int* offsets;         // [N' + 1]
+    int* perm_token;      // [T K']
+    int* perm_slot;       // [T K']
+    float *f_out, *P_out, *losses;   // balance statistics, or null
 };
 
 template <int KMAX>
@@ -107,6 +117,79 @@ __device__ __forceinline__ void epilogue_bar() {
     asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// The routing tables of a one-tile batch, by the four epilogue warps (et = 0..127, thread et = token
+// et) after the tile is routed: totals, offsets (exclusive scan, segments padded to a.pad), the
+// balance statistics and the stable permutation. The rank of token t in expert j is the number of
+// earlier tokens of the tile choosing j (a prefix popcount of j's token bitmap); these are the
+// results of the finalize and scatter kernels for the same batch, bit for bit. `scratch` is the
+// idle TMA ring. Every epilogue warp runs the whole sequence (the barriers need all four).
+__device__ __noinline__ void finish_single_tile(const RouterArgs& a, uint8_t* scratch,
+                                                const int* hist, const float* colsum,
+                                                const int* chosen, int et, int lane) {
+    const int N = a.N, K = a.K, T = a.T;
+    uint32_t* bits = reinterpret_cast<uint32_t*>(scratch);         // [N'][4]: tokens 0..127
+    int* off = reinterpret_cast<int*>(bits + 4 * kMaxRouted);       // [N' + 1]
+    float* ptot = reinterpret_cast<float*>(off + kMaxRouted + 1);   // [N']
+    float* fs = ptot + kMaxRouted;                                  // [N']
+    float* Ps = fs + kMaxRouted;                                    // [N']
+    for (int i = et; i < 4 * N; i += 128) bits[i] = 0u;
+    for (int j = et; j < N; j += 128) {
+        const float col = ((colsum[j] + colsum[kMaxRouted + j]) + colsum[2 * kMaxRouted + j]) +
+                          colsum[3 * kMaxRouted + j];
+        ptot[j] = col;
+        a.counts_out[j] = hist[j];
+        a.psum_out[j] = col;
+        balance_fp(a.dims, hist[j], col, &fs[j], &Ps[j]);
+    }
+    epilogue_bar();
+    const int t = et;
+    if (t < T)
+        for (int k = 0; k < K; ++k) {
+            const int j = chosen[t * kMaxTopK + k];
+            if (j >= 0 && j < N) atomicOr(&bits[j * 4 + (t >> 5)], 1u << (t & 31));
+        }
+    if (et < 32) {   // offsets: lane l scans experts 8l .. 8l+7 (N' <= 256)
+        int loc[8], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int j = lane * 8 + q;
+            const int v = j < N ? (a.pad > 0 ? (hist[j] + a.pad - 1) / a.pad * a.pad : hist[j]) : 0;
+            loc[q] = sum;
+            sum += v;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int j = lane * 8 + q;
+            if (j < N) off[j] = incl - sum + loc[q];
+        }
+        if (lane == 31) off[N] = incl;
+    }
+    epilogue_bar();
+    for (int j = et; j <= N; j += 128) a.offsets[j] = off[j];
+    if (et == 32 && a.losses) balance_losses(a.dims, fs, Ps, a.losses);
+    if (a.f_out)
+        for (int j = et; j < N; j += 128) {
+            a.f_out[j] = fs[j];
+            a.P_out[j] = Ps[j];
+        }
+    if (t < T)
+        for (int k = 0; k < K; ++k) {
+            int j = chosen[t * kMaxTopK + k];
+            j = (j >= 0 && j < N) ? j : 0;
+            int rank = __popc(bits[j * 4 + (t >> 5)] & ((1u << (t & 31)) - 1u));
+            for (int w = 0; w < (t >> 5); ++w) rank += __popc(bits[j * 4 + w]);
+            const int row = off[j] + rank;
+            a.perm_slot[(size_t)t * K + k] = row;
+            a.perm_token[row] = t;
+        }
+}
+
 // Routing of the 128 tokens of a tile by the four epilogue warps (thread = token): softmax over
 // the N' routed experts, top-K' by logit (lower index on ties), gates, the tile histogram and the
 // tile's per-expert affinity sums. `zc` ([n_pad][128] floats, column j of row r at j * 128 + r,
@@ -115,7 +198,7 @@ __device__ __forceinline__ void epilogue_bar() {
 template <int KMAX>
 __device__ __forceinline__ void route_tile(const RouterArgs& a, uint32_t tmem_lanes, float* zc,
                                           int tile, int quarter, int lane, float* colsum,
-                                          int* hist, const float* bias_s) {
+                                          int* hist, const float* bias_s, int* chosen) {
     const int N = a.N, K = a.K;
     const int row = quarter * 32 + lane;
     const int t = tile * RBM + row;
@@ -166,6 +249,7 @@ __device__ __forceinline__ void route_tile(const RouterArgs& a, uint32_t tmem_la
                 const float s = __expf(top.v[q] - zmax) * inv;
                 a.topk_idx[(size_t)t * K + q - q0] = j;
                 a.topk_gate[(size_t)t * K + q - q0] = a.renorm ? s / gsum : s;
+                chosen[row * kMaxTopK + q - q0] = j;   // for the one-tile tables
                 atomicAdd(&hist[j], 1);
             }
         }
@@ -294,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     int* hist = reinterpret_cast<int*>(colsum + 4 * kMaxRouted);  // [kMaxRouted]
     float* bias_s = reinterpret_cast<float*>(hist + kMaxRouted);  // [kMaxRouted]
     float* aux_s = bias_s + kMaxRouted;                           // [kMaxRouted] (backward)
+    int* chosen = reinterpret_cast<int*>(aux_s + kMaxRouted);     // [128][kMaxTopK]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x;
@@ -423,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
                                bias_s, aux_s);
             else
                 route_tile<KMAX>(a, tb, reinterpret_cast<float*>(base), tile, quarter, lane,
-                                 colsum, hist, bias_s);
+                                 colsum, hist, bias_s, chosen);
             routed_here = true;
         }
         ptx::tc_fence_before();
@@ -440,6 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
                     a.tile_counts[(size_t)j * n_tiles + tile] = hist[j];
                 }
             }
+        }
+        if constexpr (!BWD) {
+            if (a.fused) finish_single_tile(a, base, hist, colsum, chosen, et, lane);
         }
     }
 
@@ -460,6 +548,7 @@ static cudaError_t router_args(const Dims& m, const void* u, const void* centroi
         !encode_bf16_map(&a.b, centroids, (uint64_t)m.N, (uint64_t)m.d, a.n_pad))
         return cudaErrorInvalidValue;
     a.bias = bias;
+    a.dims = m;
     a.T = m.T;
     a.N = m.N;
     a.K = m.K;
@@ -477,7 +566,7 @@ static cudaError_t router_args(const Dims& m, const void* u, const void* centroi
 template <int KMAX, bool BWD>
 static cudaError_t launch_router_kernel(const Dims& m, const RouterArgs& a, cudaStream_t st) {
     const size_t smem = 1024 + (size_t)a.stages * a.stage_bytes + 8 * (2 * kMaxStages + 2) + 16 +
-                        4 * (4 * kMaxRouted + 3 * kMaxRouted);
+                        4 * (4 * kMaxRouted + 3 * kMaxRouted) + 4 * RBM * kMaxTopK;
     const int n_tiles = (m.T + RBM - 1) / RBM;
     auto kern = router_tc_kernel<KMAX, BWD>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
@@ -490,7 +579,8 @@ static cudaError_t launch_router_kernel(const Dims& m, const RouterArgs& a, cuda
 
 cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids,
                              const float* bias, int* topk_idx, float* topk_gate, int* tile_counts,
-                             float* tile_psum, int* status, cudaStream_t st) {
+                             float* tile_psum, int* status, cudaStream_t st,
+                             const SingleTileTables* tables) {
     RouterArgs a{};
     cudaError_t e = router_args(m, u, centroids, bias, a);
     if (e != cudaSuccess) return e;
@@ -499,6 +589,19 @@ cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids
     a.tile_counts = tile_counts;
     a.tile_psum = tile_psum;
     a.status = status;
+    if (tables) {
+        if (m.T > RBM) return cudaErrorInvalidValue;   // one tile only
+        a.fused = 1;
+        a.pad = tables->pad;
+        a.counts_out = tables->counts;
+        a.psum_out = tables->psum;
+        a.offsets = tables->offsets;
+        a.perm_token = tables->perm_token;
+        a.perm_slot = tables->perm_slot;
+        a.f_out = tables->f;
+        a.P_out = tables->P;
+        a.losses = tables->losses;
+    }
     return m.skip + m.K <= 8 ? launch_router_kernel<8, false>(m, a, st)
                              : launch_router_kernel<16, false>(m, a, st);
 }

@@ -253,3 +253,30 @@ def test_bounded_wait_times_out_and_context_survives():
     assert st.status() == 0
     ref = oracle.route(st.ocfg, st.inputs["u"], st.inputs["centroids"])
     check_routing(st.ocfg, ref, to_np(st.idx), to_np(st.gate), to_np(st.counts))
+
+
+@pytest.mark.parametrize("name,T", [("16b_decode_bf16", 64), ("2b_bf16", 1), ("2b_bf16", 100),
+                                    ("2b_bf16", 128), ("145b_zipf_bf16", 77)])
+def test_one_tile_layer_equals_the_stages(name, T):
+    """A batch of at most 128 tokens has one router tile, and the layer call then takes its
+    counts, offsets, permutation and balance statistics from the router itself instead of the
+    finalize and scatter kernels. Every output must equal the stage-by-stage calls' bit for bit."""
+    st = Stages(C[name], T)
+    st.route()
+    st.permute()
+    st.pack()
+    st.ffn()
+    st.combine()
+    st.stats()
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    layer = st.moe.MoELayer(st.cfg, st.inputs["centroids"], st.inputs["w_gate"],
+                            st.inputs["w_up"], st.inputs["w_down"], st.inputs["bias"])
+    h = layer.forward(st.u)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    assert torch.equal(h, st.h)
+    assert torch.equal(layer.topk_idx[:T], st.idx) and torch.equal(layer.topk_gate[:T], st.gate)
+    assert torch.equal(layer.counts, st.counts)
+    for got, want in ((layer.f, st.f), (layer.P, st.P), (layer.losses, st.losses)):
+        assert torch.equal(got, want)
