@@ -189,6 +189,34 @@ __global__ void gather_kernel(Dims m, const uint4* __restrict__ u, const int* __
     }
 }
 
+// Small batches: one CTA per token, thread i copying 16-byte vectors i, i + blockDim, ... of the
+// row to the token's K' rows, so the copy spreads over T SMs instead of T / 8.
+__global__ void gather_cta_kernel(Dims m, const uint4* __restrict__ u,
+                                  const int* __restrict__ perm_slot, uint4* __restrict__ x_perm,
+                                  int* status, long TK) {
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x;
+    const int vec_per_row = m.d * m.elem() / 16;
+    int rows[kMaxTopK];
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < kMaxTopK; ++k) {
+        rows[k] = k < m.K ? perm_slot[(size_t)t * m.K + k] : -1;
+        if (k < m.K && (rows[k] < 0 || rows[k] >= TK)) {
+            bad = true;
+            rows[k] = -1;
+        }
+    }
+    if (bad && threadIdx.x == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
+    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
+        const uint4 x = u[(size_t)t * vec_per_row + v];
+#pragma unroll
+        for (int k = 0; k < kMaxTopK; ++k)
+            if (k < m.K && rows[k] >= 0) x_perm[(size_t)rows[k] * vec_per_row + v] = x;
+    }
+}
+
 // One warp per permuted row: x_perm[r] = u[perm_token[r]] for the rows the offsets cover.
 __global__ void gather_rows_kernel(Dims m, const uint4* __restrict__ u,
                                    const int* __restrict__ offsets,
@@ -262,10 +290,19 @@ cudaError_t launch_gather(const Dims& m, const void* u, const int* perm_slot, vo
     const long rows = row_limit > 0 ? row_limit : (long)m.T * m.K;
     if (m.T == 0) return cudaSuccess;
     const int threads = 256, warps_per_block = threads / 32;
-    const int blocks = (m.T + warps_per_block - 1) / warps_per_block;
-    cudaError_t e = launch_pdl(gather_kernel, dim3(blocks), dim3(threads), 0, st, m,
-                               static_cast<const uint4*>(u), perm_slot,
-                               static_cast<uint4*>(x_perm), status, rows);
+    cudaError_t e;
+    if (m.T <= 2 * sm_count()) {   // a warp per token would leave most SMs idle
+        const int vecs = m.d * m.elem() / 16;
+        const int tpb = vecs >= 256 ? 256 : ((vecs + 31) / 32) * 32;
+        e = launch_pdl(gather_cta_kernel, dim3(m.T), dim3(tpb), 0, st, m,
+                       static_cast<const uint4*>(u), perm_slot, static_cast<uint4*>(x_perm), status,
+                       rows);
+    } else {
+        const int blocks = (m.T + warps_per_block - 1) / warps_per_block;
+        e = launch_pdl(gather_kernel, dim3(blocks), dim3(threads), 0, st, m,
+                       static_cast<const uint4*>(u), perm_slot, static_cast<uint4*>(x_perm), status,
+                       rows);
+    }
     if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
