@@ -40,8 +40,11 @@ def flops_per_token(sh) -> float:
     return 6.0 * sh.d * sh.inter * (sh.n_shared + sh.top_k) + 2.0 * sh.d * sh.n_routed
 
 
-def gate_up_flops(sh, T) -> float:
-    return 4.0 * sh.d * sh.inter * T * (sh.n_shared + sh.top_k)
+def gate_up_flops(sh, T, with_shared=True) -> float:
+    """FLOPs of the gate/up GEMM over the routed groups, plus the shared group's when
+    with_shared."""
+    shared = sh.n_shared if with_shared and not sh.drop_shared else 0
+    return 4.0 * sh.d * sh.inter * T * (shared + sh.top_k)
 
 
 def workload_config(sh, T, world, graph=False) -> dict:
@@ -55,12 +58,13 @@ def workload_config(sh, T, world, graph=False) -> dict:
             "inputs": "seeded Gaussian tensors of the workload's shape"}
 
 
-def gate_up_bytes(sh, T, counts) -> float:
-    """Algorithmic DRAM bytes of one gate/up launch: the gate and up weights of the shared
-    experts and of every routed expert that received a token, the A rows it reads (T K' routed
-    rows and, with shared experts, the T rows of u) and the activations it writes."""
+def gate_up_bytes(sh, T, counts, with_shared=True) -> float:
+    """Algorithmic DRAM bytes of one gate/up launch: the gate and up weights of every routed
+    expert that received a token (and of the shared experts when with_shared), the A rows it
+    reads (T K' routed rows and, with the shared experts, the T rows of u) and the activations
+    it writes."""
     es = 4 if sh.dtype == "f32" else 2
-    shared = sh.n_shared if not sh.drop_shared else 0
+    shared = sh.n_shared if with_shared and not sh.drop_shared else 0
     touched = int(sum(1 for c in counts if c > 0))
     weights = (shared + touched) * 2 * sh.inter * sh.d * es
     a_rows = T * sh.top_k + (T if shared else 0)
@@ -68,8 +72,9 @@ def gate_up_bytes(sh, T, counts) -> float:
     return float(weights + a_rows * sh.d * es + act)
 
 
-def gate_up_traffic(workload: str):
-    """DRAM bytes (read + write) of one gate/up GEMM launch from the committed ncu summary, or
+def gate_up_traffic(workload: str, kernel: str = "gemm_gate_up"):
+    """DRAM bytes (read + write) of one gate/up GEMM launch (`kernel`: gemm_gate_up over all
+    groups, gemm_gate_up_routed over the routed groups only) from the committed ncu summary, or
     None when the workload was not captured."""
     path = os.path.join(ROOT, "profiles", "gemm_traffic_full_size.txt")
     if not os.path.exists(path):
@@ -78,7 +83,7 @@ def gate_up_traffic(workload: str):
         for line in f:
             parts = line.split()
             if len(parts) == 5 and not line.startswith("#") and parts[0] == workload \
-                    and parts[1] == "gemm_gate_up":
+                    and parts[1] == kernel:
                 return int(parts[2]) + int(parts[3])
     return None
 
@@ -277,17 +282,15 @@ def run_ours(args, sh, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     barrier()
     launches = moe.moe_launch_count() - launches0 + graph_kernels * args.steps
-    if graph is None:
-        stage_ms, n_prof = moe.moe_profile_read()
-        moe.moe_profile_enable(False)
-    else:   # stage times come from a separate profiled pass of direct calls
+    if graph is not None:   # stage times come from a separate profiled pass of direct calls
         moe.moe_profile_enable(True, args.steps)
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             layer.forward(u)
         torch.cuda.synchronize(dev)
-        stage_ms, n_prof = moe.moe_profile_read()
-        moe.moe_profile_enable(False)
+    stage_ms, n_prof = moe.moe_profile_read()
+    gu_launch_ms, _, n_split = moe.moe_profile_read_gate_up()
+    moe.moe_profile_enable(False)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
 
@@ -346,27 +349,36 @@ def run_ours(args, sh, rank, world, local_rank):
         return
 
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = load_peaks()
-    traffic = gate_up_traffic(sh.name)
+    # the dominant launch: the gate/up GEMM over the routed groups (over every group when the
+    # shared group was not split off into a launch of its own)
+    split = n_split > 0
+    if n_split not in (0, n_prof):
+        raise RuntimeError(f"{n_split} of {n_prof} profiled calls split the gate/up GEMM")
+    traffic = gate_up_traffic(sh.name, "gemm_gate_up_routed" if split else "gemm_gate_up")
     counts_host = layer.counts.cpu().tolist()
     tokens = T * world * args.steps
     value = tokens / (total_ms / 1e3)
     e2e_value = tokens / (e2e_ms / 1e3)
-    gu_ms = stage_ms["gemm_gate_up"] / max(n_prof, 1)
-    gu_tflops = gate_up_flops(sh, T) / (gu_ms / 1e3) / 1e12
+    gu_ms = gu_launch_ms / max(n_prof, 1)
+    gu_flops = gate_up_flops(sh, T, with_shared=not split)
+    gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
     # the launch is bound by whichever of its FLOPs and its algorithmic bytes takes longer at peak
-    gu_bytes = gate_up_bytes(sh, T, counts_host)
-    hbm_bound = gu_bytes / (hbm_gbs * 1e9) > gate_up_flops(sh, T) / (bf16_tf * 1e12)
+    gu_bytes = gate_up_bytes(sh, T, counts_host, with_shared=not split)
+    hbm_bound = gu_bytes / (hbm_gbs * 1e9) > gu_flops / (bf16_tf * 1e12)
     gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
+    kernel = "gemm_tc_kernel (gate/up + SwiGLU epilogue, " + \
+        ("routed groups; the shared group runs in a launch of its own)" if split else "all groups)")
     if hbm_bound:
-        roof = {"bound": "hbm", "kernel": "gemm_tc_kernel (gate/up + SwiGLU epilogue)",
+        roof = {"bound": "hbm", "kernel": kernel,
                 "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
                 "traffic": traffic, "peak_source": f"{peak_src} HBM copy",
                 "algorithmic_bytes": gu_bytes}
     else:
-        roof = {"bound": "tensor", "kernel": "gemm_tc_kernel (gate/up + SwiGLU epilogue)",
+        roof = {"bound": "tensor", "kernel": kernel,
                 "achieved": gu_tflops, "peak": bf16_tf, "unit": "TFLOP/s",
                 "frac": gu_tflops / bf16_tf, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 burst"}
+    roof["launch_ms"] = gu_ms
     layer_tflops = flops_per_token(sh) * T / (total_ms / args.steps / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -10,6 +10,7 @@ from .binding import (MOE_DTYPE_BF16, MOE_DTYPE_F32, N_STAGES, STAGE_NAMES, MoEC
                       moe_layer_backward_saved, moe_layer_forward, moe_layer_forward_train,
                       moe_pack_weights, moe_pack_weights_backward, moe_packed_backward_bytes,
                       moe_packed_weight_bytes, moe_permute, moe_profile_enable, moe_profile_read,
+                      moe_profile_read_gate_up,
                       moe_route, moe_selftest_bounded_wait, moe_status_string,
                       moe_workspace_bytes)
 from .layer import MoELayer
@@ -20,4 +21,5 @@ __all__ = ["MOE_DTYPE_BF16", "MOE_DTYPE_F32", "N_STAGES", "STAGE_NAMES", "MoECon
            "moe_layer_backward_saved", "moe_layer_forward", "moe_layer_forward_train",
            "moe_pack_weights", "moe_pack_weights_backward", "moe_packed_backward_bytes",
            "moe_packed_weight_bytes", "moe_permute", "moe_profile_enable", "moe_profile_read",
+           "moe_profile_read_gate_up",
            "moe_route", "moe_selftest_bounded_wait", "moe_status_string", "moe_workspace_bytes"]

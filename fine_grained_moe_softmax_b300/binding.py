@@ -77,6 +77,9 @@ _SIG = {
     "moe_profile_enable": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "moe_profile_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
                                         ctypes.POINTER(ctypes.c_int)]),
+    "moe_profile_read_gate_up": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
+                                                ctypes.POINTER(ctypes.c_int),
+                                                ctypes.POINTER(ctypes.c_int)]),
 }
 
 
@@ -252,3 +255,13 @@ def moe_profile_read():
     n = ctypes.c_int()
     _check(lib().moe_profile_read(ms, ctypes.byref(n)), "moe_profile_read")
     return dict(zip(STAGE_NAMES, list(ms))), n.value
+
+
+def moe_profile_read_gate_up():
+    """(summed milliseconds of the gate/up launch over the routed groups, recorded calls, calls
+    whose shared group had a gate/up launch of its own)."""
+    ms = ctypes.c_float()
+    n, n_split = ctypes.c_int(), ctypes.c_int()
+    _check(lib().moe_profile_read_gate_up(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(n_split)),
+           "moe_profile_read_gate_up")
+    return ms.value, n.value, n_split.value

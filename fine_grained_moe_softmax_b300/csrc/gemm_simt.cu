@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(SimtArgs a) {
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
 
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const TileInfo ti = decode_tile(t, prefix, rows_s, row0_s, a.gt);
+        const TileInfo ti = decode_tile<SB>(t, prefix, rows_s, row0_s, a.gt);
         const bool sh = ti.group == 0;
         const float* A = sh ? a.a_s : a.a_r;
         const float* B = sh ? a.b_s : a.b_r + (size_t)(ti.group - 1) * a.b_rows_per_expert *
@@ -111,6 +111,7 @@ cudaError_t run_simt(const Dims& m, SimtArgs a, cudaStream_t st) {
     a.gt.max_rows_r = m.T * m.K;
     a.gt.n_tiles_r = (a.n_out_r + SB - 1) / SB;
     a.gt.n_tiles_s = m.shared_active() ? (a.n_out_s + SB - 1) / SB : 0;
+    a.gt.n_panel_s = 0;
     cudaError_t e = launch_pdl(gemm_simt_kernel<GATEUP>, dim3(4 * sm_count()), dim3(256), 0, st, a);
     if (e != cudaSuccess) return e;
     note_launches(1);

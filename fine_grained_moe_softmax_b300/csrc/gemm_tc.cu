@@ -241,7 +241,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             long issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, prefix, rows_s, row0_s, gt);
+                const TileInfo ti = decode_tile<BM>(t, prefix, rows_s, row0_s, gt);
                 const bool sh = ti.group == 0;
                 const CUtensorMap* am = sh ? &args.a_s : &args.a_r;
                 const CUtensorMap* bm = sh ? &args.b_s : &args.b_r;
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, any = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, prefix, rows_s, row0_s, gt);
+                const TileInfo ti = decode_tile<BM>(t, prefix, rows_s, row0_s, gt);
                 const int kb_n = ti.group == 0 ? args.k_blocks_s : args.k_blocks_r;
                 if (!wait_phase(ptx::smem_addr(&tempty[acc]), acc_phase ^ 1, abort_flag,
                                 args.status))
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const TileInfo ti = decode_tile(t, prefix, rows_s, row0_s, gt);
+            const TileInfo ti = decode_tile<BM>(t, prefix, rows_s, row0_s, gt);
             const bool sh = ti.group == 0;
             const int r = ti.m_blk * BM + quarter * 32 + lane;     // row inside the group
             const bool valid = r < ti.m_rows;
@@ -581,6 +581,11 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     a.gt.max_rows_r = (int)std::min<uint64_t>(g.a_rows_r, INT32_MAX);
     a.gt.n_tiles_r = (g.n_cols_r + bn - 1) / bn;
     a.gt.n_tiles_s = shared ? (g.n_cols_s + bn - 1) / bn : 0;
+    // Shared-group weights above 64 MB do not stay in L2 while all row blocks pass over them:
+    // panels of about 32 MB of weights each, so that A is read once per panel instead.
+    const uint64_t b_col_bytes = (uint64_t)bn * g.k_s * 2;
+    if (shared && (uint64_t)a.gt.n_tiles_s * b_col_bytes > (64ull << 20))
+        a.gt.n_panel_s = (int)std::max<uint64_t>(1, (32ull << 20) / b_col_bytes);
     a.k_blocks_r = (int)((g.k_r + BK - 1) / BK);
     a.k_blocks_s = shared ? (int)((g.k_s + BK - 1) / BK) : 0;
     a.b_rows_per_expert = g.b_rows_per_expert;
@@ -629,14 +634,23 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
 cudaError_t launch_expert_gemms(const Dims& m, const void* u, const void* x_perm,
                                 const void* packed, const int* offsets, void* act_r, void* act_s,
                                 void* y_r, void* y_s, int* status, cudaStream_t st,
-                                cudaEvent_t mid_event) {
+                                cudaEvent_t mid_event, cudaEvent_t routed_ready,
+                                cudaEvent_t main_start) {
     if (m.T == 0) {
+        if (routed_ready) cudaStreamWaitEvent(st, routed_ready, 0);
+        if (main_start) cudaEventRecord(main_start, st);
         if (mid_event) cudaEventRecord(mid_event, st);
         return cudaSuccess;
     }
-    if (m.dtype == MOE_DTYPE_F32)
+    if (m.dtype == MOE_DTYPE_F32) {
+        if (routed_ready) {
+            const cudaError_t e = cudaStreamWaitEvent(st, routed_ready, 0);
+            if (e != cudaSuccess) return e;
+        }
+        if (main_start) cudaEventRecord(main_start, st);
         return launch_expert_gemms_simt(m, u, x_perm, packed, offsets, act_r, act_s, y_r, y_s, st,
                                         mid_event);
+    }
     const PackLayout P = pack_layout(m);
     const char* pk = static_cast<const char*>(packed);
     const uint64_t TK = (uint64_t)m.T * m.K, KsI = (uint64_t)m.Ks * m.I;
@@ -662,7 +676,25 @@ cudaError_t launch_expert_gemms(const Dims& m, const void* u, const void* x_perm
     gu.out_s = act_s;
     gu.ld_r = m.I;
     gu.ld_s = (int)KsI;
-    cudaError_t e = run_gemm<1>(gu, status, st);
+    cudaError_t e;
+    if (routed_ready && gu.has_shared) {
+        // the shared group needs only u: it runs first, while the routed rows are being gathered
+        // on another stream; the routed groups follow once routed_ready has completed
+        GroupedGemm gs = gu;
+        gs.n_routed = 0;
+        e = run_gemm<1>(gs, status, st);
+        const cudaError_t ew = cudaStreamWaitEvent(st, routed_ready, 0);   // also after an error
+        if (e == cudaSuccess) e = ew;
+        GroupedGemm gr = gu;
+        gr.has_shared = 0;
+        if (main_start) cudaEventRecord(main_start, st);
+        if (e == cudaSuccess) e = run_gemm<1>(gr, status, st);
+    } else {
+        if (routed_ready) e = cudaStreamWaitEvent(st, routed_ready, 0);
+        else e = cudaSuccess;
+        if (main_start) cudaEventRecord(main_start, st);
+        if (e == cudaSuccess) e = run_gemm<1>(gu, status, st);
+    }
     if (e != cudaSuccess) return e;
     if (mid_event) cudaEventRecord(mid_event, st);
     GroupedGemm dn = gu;

@@ -5,6 +5,10 @@
 // A group of M rows and Nc output columns has ceil(M/BM) * ceil(Nc/BN) tiles, enumerated with the
 // column tile fastest so that CTAs running at the same time share the group's A rows and weights
 // through L2. Tile t of the whole launch belongs to the group g with prefix[g] <= t < prefix[g+1].
+// When the shared group's weights are too large to stay in L2 while every row block passes over
+// them, its column tiles are cut into panels of n_panel_s columns, enumerated one after another
+// (all row blocks of a panel, column fastest, before the next panel): the weights of a panel stay
+// in L2 and A is read once per panel.
 #pragma once
 
 #include "common.cuh"
@@ -18,6 +22,7 @@ struct GroupTiles {
     int n_tiles_r;     // column tiles of a routed group
     int n_tiles_s;     // column tiles of the shared group
     int max_rows_r;    // rows of the routed A / output matrices
+    int n_panel_s;     // column tiles per panel of the shared group (<= 0: one panel)
 };
 
 struct TileInfo {
@@ -68,6 +73,7 @@ __device__ __forceinline__ void build_tile_prefix(int* prefix, int* rows_s, int*
     __syncthreads();
 }
 
+template <int BM>
 __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const int* rows_s,
                                                 const int* row0_s, const GroupTiles& gt) {
     int lo = 0, hi = gt.n_groups - 1;   // find g with prefix[g] <= t < prefix[g+1]
@@ -82,8 +88,20 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const 
     ti.row0 = row0_s[lo];
     const int nt = lo == 0 ? gt.n_tiles_s : gt.n_tiles_r;
     const int local = t - prefix[lo];
-    ti.m_blk = local / nt;
-    ti.n_blk = local % nt;
+    const int pw = lo == 0 && gt.n_panel_s > 0 && gt.n_panel_s < nt ? gt.n_panel_s : nt;
+    if (pw == nt) {
+        ti.m_blk = local / nt;
+        ti.n_blk = local % nt;
+    } else {
+        const int mb = (ti.m_rows + BM - 1) / BM;
+        const int full = nt / pw;                 // panels of pw columns, then one narrower
+        const int per_panel = mb * pw;
+        const int p = min(local / per_panel, full);
+        const int w = p < full ? pw : nt - full * pw;
+        const int r = local - p * per_panel;
+        ti.m_blk = r / w;
+        ti.n_blk = p * pw + r % w;
+    }
     return ti;
 }
 

@@ -81,10 +81,15 @@ cudaError_t launch_gather_rows(const Dims& m, const void* u, const int* offsets,
 // Expert GEMMs (gate/up with the SwiGLU epilogue, then down), routed groups from offsets plus one
 // dense shared group. x_perm and u are the A operands of gate/up; act_r/act_s are written, then
 // read by the down GEMM which writes y_r / y_s.
+// With routed_ready, the shared group's gate/up runs first and the routed groups' only after
+// that event (the permuted rows are produced on another stream meanwhile). Optional events:
+// main_start is recorded right before the gate/up launch over the routed groups, mid_event after
+// the gate/up work.
 cudaError_t launch_expert_gemms(const Dims& m, const void* u, const void* x_perm,
                                 const void* packed, const int* offsets, void* act_r, void* act_s,
                                 void* y_r, void* y_s, int* status, cudaStream_t st,
-                                cudaEvent_t mid_event);
+                                cudaEvent_t mid_event, cudaEvent_t routed_ready = nullptr,
+                                cudaEvent_t main_start = nullptr);
 
 // One launch of the tensor-core grouped GEMM (bf16 in, fp32 accumulate, bf16 out): group 0 is a
 // dense group of T_shared rows (when has_shared), groups 1..n_routed the routed experts (rows

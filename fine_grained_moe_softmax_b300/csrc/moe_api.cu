@@ -27,6 +27,38 @@ int sm_count() {
     return cached[dev];
 }
 
+// Per-device side stream of the layer call and its fork / join events, created on first use (the
+// first call on a device, before any graph capture of it). fork_join_mutex keeps one call's
+// fork-join section from interleaving with another host thread's.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+std::mutex& fork_join_mutex() {
+    static std::mutex mu;
+    return mu;
+}
+
+cudaError_t side_stream(SideStream** out) {
+    static std::mutex mu;
+    static SideStream per_dev[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    SideStream& ss = per_dev[dev];
+    if (!ss.s) {
+        if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess)
+            return e;
+    }
+    *out = &ss;
+    return cudaSuccess;
+}
+
 cudaError_t ensure_smem(const void* func, size_t bytes) {
     static std::mutex mu;
     static std::vector<std::pair<std::pair<const void*, int>, size_t>> granted;
@@ -97,32 +129,42 @@ template <typename T> T* at(void* ws, size_t off) {
 
 // ------------------------------------------------------------------- stage timing ----
 
+// Per recorded call: the MOE_N_STAGES + 1 stage boundaries, then the start of the gate/up launch
+// over the routed groups (kEvPerCall events), and whether the shared group had a launch of its own.
+constexpr int kEvPerCall = MOE_N_STAGES + 2;
 struct Profile {
     std::mutex mu;
     bool on = false;
     int max_calls = 0, recorded = 0;
-    std::vector<cudaEvent_t> ev;   // (MOE_N_STAGES + 1) per call
+    std::vector<cudaEvent_t> ev;
+    std::vector<char> split;
 };
 Profile g_prof;
 
 void free_profile_events() {
     for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
     g_prof.ev.clear();
+    g_prof.split.clear();
     g_prof.recorded = 0;
 }
 
 // Events of the next recorded call, or null when not profiling / out of slots.
-cudaEvent_t* profile_slot() {
+cudaEvent_t* profile_slot(char** split) {
     std::lock_guard<std::mutex> lock(g_prof.mu);
+    *split = nullptr;
     if (!g_prof.on || g_prof.recorded >= g_prof.max_calls) return nullptr;
-    return &g_prof.ev[(size_t)(g_prof.recorded++) * (MOE_N_STAGES + 1)];
+    const int c = g_prof.recorded++;
+    *split = &g_prof.split[c];
+    return &g_prof.ev[(size_t)c * kEvPerCall];
 }
 
 struct Marks {
     cudaEvent_t* ev;
+    char* split;
     cudaStream_t st;
-    void mark(int i) {
-        if (ev) cudaEventRecord(ev[i], st);
+    void mark(int i) { mark_on(i, st); }
+    void mark_on(int i, cudaStream_t s) {
+        if (ev) cudaEventRecord(ev[i], s);
     }
     cudaEvent_t at(int i) { return ev ? ev[i] : nullptr; }
 };
@@ -293,7 +335,8 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
     int* offsets = at<int>(ws, L.offsets);
     int* perm_token = at<int>(ws, L.perm_token);
     int* perm_slot = at<int>(ws, L.perm_slot);
-    Marks mk{profile_slot(), st};
+    Marks mk{nullptr, nullptr, st};
+    mk.ev = profile_slot(&mk.split);
 
     if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
     mk.mark(0);
@@ -325,12 +368,39 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
     if (e == cudaSuccess && !one_tile)
         e = launch_perm_scatter(m, topk_idx, offsets, tb, perm_token, perm_slot, st);
     mk.mark(2);
-    if (e == cudaSuccess) e = launch_gather(m, u, perm_slot, at<void>(ws, L.x_perm), status, st);
-    mk.mark(3);
-    if (e == cudaSuccess)
+    // With shared experts, the shared group's gate/up GEMM needs only u. The permuted token rows
+    // are then gathered on a side stream while it runs (the gather needs no shared memory, so its
+    // CTAs fit beside the GEMM's, and the GEMM leaves most of the memory bandwidth idle); the
+    // routed groups' gate/up follows once they are ready. The gather stage of the profile is then
+    // timed on the side stream and the gate/up stage is the rest of the gate/up work.
+    const bool overlap = e == cudaSuccess && !one_tile && m.dtype == MOE_DTYPE_BF16 &&
+                         m.shared_active();
+    SideStream* ss = nullptr;
+    if (overlap && (e = side_stream(&ss)) != cudaSuccess) return cuda_rc(e);
+    std::unique_lock<std::mutex> fj(fork_join_mutex(), std::defer_lock);
+    cudaStream_t sst = st;   // the stream of the gather
+    if (overlap) {
+        fj.lock();
+        sst = ss->s;
+        if ((e = cudaEventRecord(ss->fork, st)) == cudaSuccess)
+            e = cudaStreamWaitEvent(sst, ss->fork, 0);
+    }
+    if (e == cudaSuccess) e = launch_gather(m, u, perm_slot, at<void>(ws, L.x_perm), status, sst);
+    mk.mark_on(3, sst);
+    bool joined = !overlap;
+    if (overlap) {
+        const cudaError_t ej = cudaEventRecord(ss->join, sst);
+        if (e == cudaSuccess) e = ej;
+    }
+    if (mk.split) *mk.split = overlap;
+    if (e == cudaSuccess) {
+        joined = true;   // the routed gate/up launch waits for the join event
         e = launch_expert_gemms(m, u, at<void>(ws, L.x_perm), packed_w, offsets,
                                 at<void>(ws, L.act_r), at<void>(ws, L.act_s), at<void>(ws, L.y_r),
-                                at<void>(ws, L.y_s), status, st, mk.at(4));
+                                at<void>(ws, L.y_s), status, st, mk.at(4),
+                                overlap ? ss->join : nullptr, mk.at(MOE_N_STAGES + 1));
+    }
+    if (!joined) cudaStreamWaitEvent(st, ss->join, 0);   // an error: still end the fork on st
     mk.mark(5);
     if (e == cudaSuccess)
         e = launch_combine(m, u, at<void>(ws, L.y_r), at<void>(ws, L.y_s), perm_slot, topk_gate, h,
@@ -382,7 +452,8 @@ int moe_profile_enable(int enable, int max_calls) {
     g_prof.on = false;
     if (!enable) return MOE_OK;
     if (max_calls <= 0) return MOE_ERR_INVALID_ARG;
-    g_prof.ev.resize((size_t)max_calls * (MOE_N_STAGES + 1));
+    g_prof.ev.resize((size_t)max_calls * kEvPerCall);
+    g_prof.split.assign((size_t)max_calls, 0);
     for (auto& e : g_prof.ev)
         if (cudaEventCreate(&e) != cudaSuccess) {
             e = nullptr;
@@ -399,13 +470,31 @@ int moe_profile_read(float* ms, int* n_calls) {
     std::lock_guard<std::mutex> lock(g_prof.mu);
     for (int s = 0; s < MOE_N_STAGES; ++s) ms[s] = 0.f;
     for (int c = 0; c < g_prof.recorded; ++c) {
-        cudaEvent_t* ev = &g_prof.ev[(size_t)c * (MOE_N_STAGES + 1)];
+        cudaEvent_t* ev = &g_prof.ev[(size_t)c * kEvPerCall];
         if (cudaEventSynchronize(ev[MOE_N_STAGES]) != cudaSuccess) return MOE_ERR_CUDA;
         for (int s = 0; s < MOE_N_STAGES; ++s) {
             float t = 0.f;
             if (cudaEventElapsedTime(&t, ev[s], ev[s + 1]) != cudaSuccess) return MOE_ERR_CUDA;
             ms[s] += t;
         }
+    }
+    *n_calls = g_prof.recorded;
+    return MOE_OK;
+}
+
+int moe_profile_read_gate_up(float* ms, int* n_calls, int* n_split) {
+    if (!ms || !n_calls || !n_split) return MOE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    *ms = 0.f;
+    *n_split = 0;
+    for (int c = 0; c < g_prof.recorded; ++c) {
+        cudaEvent_t* ev = &g_prof.ev[(size_t)c * kEvPerCall];
+        if (cudaEventSynchronize(ev[MOE_N_STAGES]) != cudaSuccess) return MOE_ERR_CUDA;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, ev[MOE_N_STAGES + 1], ev[4]) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        *ms += t;
+        *n_split += g_prof.split[c];
     }
     *n_calls = g_prof.recorded;
     return MOE_OK;

@@ -238,13 +238,23 @@ uint64_t moe_launch_count(void);
 
 /* Per-stage timing of moe_layer_forward. enable != 0 starts recording a CUDA event around each
  * stage (router, permute, gather, gate/up GEMM, down GEMM, combine, statistics) of the next
- * calls, up to max_calls of them; enable == 0 stops and frees the events. */
+ * calls, up to max_calls of them; enable == 0 stops and frees the events. When a bf16 call with
+ * shared experts and more than one router tile splits its gate/up GEMM (the shared group first,
+ * beside the gather on a second stream, then the routed groups), the gather stage is its time on
+ * the second stream and the gate/up stage is the time from the end of the gather to the end of
+ * the routed groups' launch; the stages still add up to the call. */
 int moe_profile_enable(int enable, int max_calls);
 
 /* Waits for the recorded events and writes, per stage, the summed milliseconds over the recorded
  * calls into ms[0 .. MOE_N_STAGES-1]; *n_calls receives the number of calls recorded. */
 #define MOE_N_STAGES 7
 int moe_profile_read(float* ms, int* n_calls);
+
+/* Summed milliseconds, over the recorded calls, of the gate/up GEMM launch that covers the routed
+ * groups (it also covers the shared group in calls that did not split it off), from its start on
+ * the call's stream to its end. *n_calls: calls recorded; *n_split: how many of them split the
+ * shared group into a launch of its own. */
+int moe_profile_read_gate_up(float* ms, int* n_calls, int* n_split);
 
 #ifdef __cplusplus
 }

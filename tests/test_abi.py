@@ -14,7 +14,8 @@ from fine_grained_moe_softmax_b300 import build as build_mod  # noqa: E402
 EXPECTED = {"moe_workspace_bytes", "moe_packed_weight_bytes", "moe_pack_weights", "moe_route",
             "moe_permute", "moe_expert_ffn", "moe_combine", "moe_balance_stats",
             "moe_layer_forward", "moe_device_status", "moe_status_string", "moe_launch_count",
-            "moe_profile_enable", "moe_profile_read", "moe_selftest_bounded_wait"}
+            "moe_profile_enable", "moe_profile_read", "moe_profile_read_gate_up",
+            "moe_selftest_bounded_wait"}
 
 
 @pytest.fixture(scope="module")
@@ -109,3 +110,8 @@ def test_profile_read_without_calls(lib):
     n = ctypes.c_int(-1)
     assert lib.moe_profile_read(ms, ctypes.byref(n)) == 0
     assert n.value == 0 and list(ms) == [0.0] * B.N_STAGES
+    gu, n_split = ctypes.c_float(-1.0), ctypes.c_int(-1)
+    assert lib.moe_profile_read_gate_up(ctypes.byref(gu), ctypes.byref(n),
+                                        ctypes.byref(n_split)) == 0
+    assert n.value == 0 and n_split.value == 0 and gu.value == 0.0
+    assert lib.moe_profile_read_gate_up(None, ctypes.byref(n), ctypes.byref(n_split)) == -1

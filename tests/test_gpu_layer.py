@@ -91,6 +91,8 @@ def _custom(**kw):
     dict(d=128, inter=320, T=200),                  # 160-column gate/up tiles
     dict(d=256, inter=128, T=40),                   # <= 64 tokens: 64-row A tiles, 5 stages
     dict(n_routed=256, top_k=8, n_groups=8, T=300), # widest router
+    # 75 MB of shared gate/up weights: column panels of the shared group, the last one narrower
+    dict(d=2048, n_shared=9, inter=1024, T=300),
     dict(dtype="f32", renormalize=1, n_shared=2),
     dict(dtype="f32", top_k=16, n_routed=16, T=77),
     # ablations of the expert-specialisation analysis: disabled top experts / shared experts

@@ -280,3 +280,57 @@ def test_one_tile_layer_equals_the_stages(name, T):
     assert torch.equal(layer.counts, st.counts)
     for got, want in ((layer.f, st.f), (layer.P, st.P), (layer.losses, st.losses)):
         assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("name,T", [("2b_bf16", 300), ("16b_bf16", 1000), ("145b_zipf_bf16", 129)])
+def test_split_gate_up_layer_equals_the_stages(name, T):
+    """With shared experts and more than one router tile, the layer call runs the shared group's
+    gate/up GEMM by itself while the gather runs on a second stream, then the
+    routed groups' gate/up. Every output must equal the stage-by-stage calls (one gate/up launch
+    over all groups) bit for bit, and the profile must report the split."""
+    st = Stages(C[name], T)
+    st.route()
+    st.permute()
+    st.pack()
+    st.ffn()
+    st.combine()
+    st.stats()
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    layer = st.moe.MoELayer(st.cfg, st.inputs["centroids"], st.inputs["w_gate"],
+                            st.inputs["w_up"], st.inputs["w_down"], st.inputs["bias"])
+    st.moe.moe_profile_enable(True, 4)
+    try:
+        for _ in range(2):
+            h = layer.forward(st.u)
+        torch.cuda.synchronize()
+        stage_ms, n = st.moe.moe_profile_read()
+        gu_ms, n_gu, n_split = st.moe.moe_profile_read_gate_up()
+    finally:
+        st.moe.moe_profile_enable(False)
+    assert layer.device_status() == 0
+    assert torch.equal(h, st.h)
+    assert torch.equal(layer.topk_idx[:T], st.idx) and torch.equal(layer.topk_gate[:T], st.gate)
+    assert torch.equal(layer.counts, st.counts)
+    for got, want in ((layer.f, st.f), (layer.P, st.P), (layer.losses, st.losses)):
+        assert torch.equal(got, want)
+    assert n == n_gu == 2 and n_split == 2
+    assert all(v >= 0 for v in stage_ms.values())
+    assert 0 < gu_ms <= stage_ms["gemm_gate_up"] + 1e-3
+
+
+def test_profile_reports_unsplit_gate_up():
+    """A one-tile batch (and a layer without shared experts) keeps one gate/up launch."""
+    st = Stages(C["16b_decode_bf16"], 64)
+    layer = st.moe.MoELayer(st.cfg, st.inputs["centroids"], st.inputs["w_gate"],
+                            st.inputs["w_up"], st.inputs["w_down"], st.inputs["bias"])
+    st.moe.moe_profile_enable(True, 2)
+    try:
+        layer.forward(st.u)
+        torch.cuda.synchronize()
+        stage_ms, n = st.moe.moe_profile_read()
+        gu_ms, n_gu, n_split = st.moe.moe_profile_read_gate_up()
+    finally:
+        st.moe.moe_profile_enable(False)
+    assert n == n_gu == 1 and n_split == 0
+    assert 0 < gu_ms <= stage_ms["gemm_gate_up"] + 1e-3
