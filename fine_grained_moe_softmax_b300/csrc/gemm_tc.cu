@@ -122,11 +122,14 @@ constexpr uint32_t staging_bytes(int epi) { return epi == 2 ? 0 : 4 * 2 * out_bo
 // rows, so its A slot holds 64 rows (8 KB) and the ring gets one more stage; the MMA still reads
 // 128 rows, the other 64 from the shared memory that follows (in bounds), and those rows' outputs
 // are never stored (an output row depends only on its own A row).
-template <int BN, int STAGES, int EPI, int ABOX = BM>
+// PAIR: the tile is computed by a CTA pair (below); each CTA holds its 128 rows of A and half of
+// the tile's BN weight rows.
+template <int BN, int STAGES, int EPI, int ABOX = BM, bool PAIR = false>
 struct Smem {
     static_assert(ABOX == BM || ABOX == 64, "A rows per tile");
+    static_assert(!PAIR || ABOX == BM, "pairs load whole 128-row A tiles");
     static constexpr uint32_t a_bytes = ABOX * BK * 2;
-    static constexpr uint32_t b_bytes = BN * BK * 2;
+    static constexpr uint32_t b_bytes = (PAIR ? BN / 2 : BN) * BK * 2;
     static constexpr uint32_t ring = STAGES * (a_bytes + b_bytes);
     static constexpr uint32_t staging = staging_bytes(EPI);
     static constexpr uint32_t bars = 8 * (2 * STAGES + 5);
@@ -166,7 +169,15 @@ __device__ __forceinline__ void load_pre_chunk(uint4 (&buf)[8], const __nv_bfloa
 // EPI: 0 plain bf16 store; 1 SwiGLU of packed gate/up column pairs (expert FFN forward);
 // 2 SwiGLU backward: the accumulator is d_act, and with the saved gate/up values of the same rows
 // (pre, packed) the epilogue writes d_gate / d_up (packed) to out.
-template <int BN, int STAGES, int EPI, int EW, int ABOX>
+//
+// PAIR: the grid is made of clusters of two CTAs on neighbouring SMs, and each pair computes
+// 256-row tiles with the CTA-pair form of the MMA. Each CTA loads its own 128 rows of A and half
+// of the BN weight rows, so an SM reads 32 KB instead of 48 KB per 64-deep K block, and the ring
+// has room for more stages. The even CTA issues the MMAs; both CTAs' loads count on its "full"
+// barriers, its MMA completions arrive on both CTAs' "empty" and "tfull" barriers, and both CTAs'
+// epilogue warps arrive on its "tempty" barriers. Each CTA's epilogue reads its own 128 rows of
+// the accumulator from its own TMEM.
+template <int BN, int STAGES, int EPI, int EW, int ABOX, bool PAIR>
 __global__ void __launch_bounds__((2 + EW) * 32, 1)
     gemm_tc_kernel(const __grid_constant__ TcArgs args) {
     static_assert(EW == 4 || EW == 8, "4 or 8 epilogue warps");
@@ -174,7 +185,9 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                   "tile width: the MMA's N (a multiple of 16 up to 256), whole 32-column chunks");
     // two accumulators of BN columns; allocations are powers of two
     constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256u : 512u;
-    using S = Smem<BN, STAGES, EPI, ABOX>;
+    static_assert(!PAIR || (EPI != 2 && BN % 32 == 0), "pair tiles: forward epilogues");
+    constexpr int TM = PAIR ? 2 * BM : BM;   // rows of a tile
+    using S = Smem<BN, STAGES, EPI, ABOX, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -195,6 +208,11 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const GroupTiles gt = args.gt;
+    const uint32_t crank = PAIR ? ptx::cluster_ctarank() : 0;   // CTA of the pair
+    const bool leader = crank == 0;
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;   // this CTA's tile stream
+    const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int row_off = (int)crank * BM;   // this CTA's rows inside a tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -203,7 +221,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_addr(&tfull[a]), 1);
-            ptx::mbar_init(ptx::smem_addr(&tempty[a]), EW);
+            ptx::mbar_init(ptx::smem_addr(&tempty[a]), PAIR ? 2 * EW : EW);
         }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
@@ -220,15 +238,23 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), kTmemCols);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_addr(tmem_holder), kTmemCols);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_addr(tmem_holder), kTmemCols);
+            ptx::tmem_relinquish();
+        }
     }
     pdl_wait();
     pdl_trigger();
-    build_tile_prefix<BM>(prefix, rows_s, row0_s, args.offsets, gt, args.counts,
+    build_tile_prefix<TM>(prefix, rows_s, row0_s, args.offsets, gt, args.counts,
                           args.status);   // syncs
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR)
+        ptx::cluster_sync();   // both CTAs' barriers are initialised before either uses the other's
+    else
+        __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const int total = prefix[gt.n_groups];
@@ -240,26 +266,37 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             uint32_t phase = 0;
             long issued = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<BM>(t, prefix, rows_s, row0_s, gt);
+            for (int t = unit; t < total && ok; t += n_units) {
+                const TileInfo ti = decode_tile<TM>(t, prefix, rows_s, row0_s, gt);
                 const bool sh = ti.group == 0;
                 const CUtensorMap* am = sh ? &args.a_s : &args.a_r;
                 const CUtensorMap* bm = sh ? &args.b_s : &args.b_r;
                 const int kb_n = sh ? args.k_blocks_s : args.k_blocks_r;
-                const int a_y = ti.row0 + ti.m_blk * BM;
-                const int b_y = (sh ? 0 : (ti.group - 1) * args.b_rows_per_expert) + ti.n_blk * BN;
+                const int a_y = ti.row0 + ti.m_blk * TM + row_off;
+                const int b_y = (sh ? 0 : (ti.group - 1) * args.b_rows_per_expert) + ti.n_blk * BN +
+                                (PAIR ? (int)crank * (BN / 2) : 0);
                 for (int kb = 0; kb < kb_n; ++kb) {
-                    if (!wait_phase(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag,
-                                    args.status)) {
+                    if (!wait_phase<PAIR>(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag,
+                                          args.status)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = ptx::smem_addr(&full[stage]);
-                    ptx::mbar_arrive_expect_tx(fb, S::a_bytes + S::b_bytes);
-                    ptx::tma_load_2d(ptx::smem_addr(a_ring + stage * S::a_bytes), am, kb * BK, a_y,
-                                     fb);
-                    ptx::tma_load_2d(ptx::smem_addr(b_ring + stage * S::b_bytes), bm, kb * BK, b_y,
-                                     fb);
+                    if constexpr (PAIR) {
+                        // both CTAs' boxes count on the even CTA's barrier, which expects them all
+                        if (leader) ptx::mbar_arrive_expect_tx(fb, 2 * (S::a_bytes + S::b_bytes));
+                        const uint32_t cfb = leader ? fb : ptx::mapa(fb, 0);
+                        ptx::tma_load_2d_pair(ptx::smem_addr(a_ring + stage * S::a_bytes), am,
+                                              kb * BK, a_y, cfb);
+                        ptx::tma_load_2d_pair(ptx::smem_addr(b_ring + stage * S::b_bytes), bm,
+                                              kb * BK, b_y, cfb);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(fb, S::a_bytes + S::b_bytes);
+                        ptx::tma_load_2d(ptx::smem_addr(a_ring + stage * S::a_bytes), am, kb * BK,
+                                         a_y, fb);
+                        ptx::tma_load_2d(ptx::smem_addr(b_ring + stage * S::b_bytes), bm, kb * BK,
+                                         b_y, fb);
+                    }
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -267,34 +304,49 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                     }
                 }
             }
-            if (!ok) {
-                // let the loads already issued land before the CTA can exit
+            if (PAIR && ok) {
+                // the even CTA's MMA completions arrive on this CTA's "empty" barriers: wait for
+                // the last ones so that none arrives after the pair has exited
+                int st2 = stage;
+                uint32_t ph2 = phase;
                 for (long i = 0; i < issued && i < STAGES; ++i) {
+                    if (--st2 < 0) {
+                        st2 = STAGES - 1;
+                        ph2 ^= 1;
+                    }
+                    drain_wait<PAIR>(ptx::smem_addr(&empty[st2]), ph2);
+                }
+            }
+            if (!ok) {
+                // let the loads already issued land before the CTA can exit (the odd CTA of a
+                // pair cannot observe its loads: it waits a fixed time before the exit instead)
+                for (long i = 0; i < issued && i < STAGES && leader; ++i) {
                     if (--stage < 0) {
                         stage = STAGES - 1;
                         phase ^= 1;
                     }
-                    drain_wait(ptx::smem_addr(&full[stage]), phase);
+                    drain_wait<PAIR>(ptx::smem_addr(&full[stage]), phase);
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------- MMA issuer ----
-        if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(TM, BN);
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, any = false;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<BM>(t, prefix, rows_s, row0_s, gt);
+            for (int t = unit; t < total && ok; t += n_units) {
+                const TileInfo ti = decode_tile<TM>(t, prefix, rows_s, row0_s, gt);
                 const int kb_n = ti.group == 0 ? args.k_blocks_s : args.k_blocks_r;
-                if (!wait_phase(ptx::smem_addr(&tempty[acc]), acc_phase ^ 1, abort_flag,
-                                args.status))
+                if (!wait_phase<PAIR>(ptx::smem_addr(&tempty[acc]), acc_phase ^ 1, abort_flag,
+                                      args.status))
                     break;
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + acc * BN;
                 for (int kb = 0; kb < kb_n; ++kb) {
-                    if (!wait_phase(ptx::smem_addr(&full[stage]), phase, abort_flag, args.status)) {
+                    if (!wait_phase<PAIR>(ptx::smem_addr(&full[stage]), phase, abort_flag,
+                                          args.status)) {
                         ok = false;
                         break;
                     }
@@ -302,27 +354,40 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                     const uint32_t a0 = ptx::smem_addr(a_ring + stage * S::a_bytes);
                     const uint32_t b0 = ptx::smem_addr(b_ring + stage * S::b_bytes);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        ptx::mma_f16(d_tmem, ptx::sw128_kmajor_desc(a0 + k * 32),
-                                     ptx::sw128_kmajor_desc(b0 + k * 32), idesc,
-                                     (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = ptx::sw128_kmajor_desc(a0 + k * 32);
+                        const uint64_t bd = ptx::sw128_kmajor_desc(b0 + k * 32);
+                        if constexpr (PAIR)
+                            ptx::mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        else
+                            ptx::mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
                     any = true;
-                    ptx::mma_commit(ptx::smem_addr(&empty[stage]));
+                    if constexpr (PAIR)
+                        ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), 3);
+                    else
+                        ptx::mma_commit(ptx::smem_addr(&empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit(ptx::smem_addr(&tfull[acc]));
+                if constexpr (PAIR)
+                    ptx::mma_commit_pair(ptx::smem_addr(&tfull[acc]), 3);
+                else
+                    ptx::mma_commit(ptx::smem_addr(&tfull[acc]));
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1;
                 }
             }
             if (*abort_flag && any) {   // make sure no MMA is still writing TMEM
-                ptx::mma_commit(ptx::smem_addr(drain));
-                drain_wait(ptx::smem_addr(drain), 0);
+                if constexpr (PAIR)
+                    ptx::mma_commit_pair(ptx::smem_addr(drain), 1);
+                else
+                    ptx::mma_commit(ptx::smem_addr(drain));
+                drain_wait<PAIR>(ptx::smem_addr(drain), 0);
             }
         }
     } else {
@@ -335,10 +400,11 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         int sbuf = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const TileInfo ti = decode_tile<BM>(t, prefix, rows_s, row0_s, gt);
+        for (int t = unit; t < total; t += n_units) {
+            const TileInfo ti = decode_tile<TM>(t, prefix, rows_s, row0_s, gt);
             const bool sh = ti.group == 0;
-            const int r = ti.m_blk * BM + quarter * 32 + lane;     // row inside the group
+            const int wrow0 = ti.m_blk * TM + row_off + quarter * 32;   // the warp's first row
+            const int r = wrow0 + lane;                                  // row inside the group
             const bool valid = r < ti.m_rows;
             __nv_bfloat16* out = sh ? args.out_s : args.out_r;
             const int ld = sh ? args.ld_s : args.ld_r;
@@ -347,7 +413,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             const int col_base = ti.n_blk * BN + c_first * 32;
             // all 32 rows of this warp lie inside the group: the box store cannot reach rows of
             // the next group
-            const bool box_store = EPI != 2 && ti.m_blk * BM + quarter * 32 + 32 <= ti.m_rows;
+            const bool box_store = EPI != 2 && wrow0 + 32 <= ti.m_rows;
             // EPI 2 reads the saved gate/up values of its rows one chunk ahead, the first chunk
             // before the accumulator is ready, so that their DRAM latency overlaps the main loop
             // and the previous chunk's arithmetic.
@@ -358,7 +424,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                 load_pre_chunk(pre_buf[0], pre_in, pre_rows, ti.row0 + r, col_base, n_cols, valid);
             int ok = 1;
             if (lane == 0)
-                ok = wait_phase(ptx::smem_addr(&tfull[acc]), acc_phase, abort_flag, args.status);
+                ok = wait_phase<PAIR>(ptx::smem_addr(&tfull[acc]), acc_phase, abort_flag,
+                                      args.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             ptx::tc_fence_after();
@@ -414,7 +481,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                         __syncwarp();
                         if (lane == 0) {
                             ptx::tma_store_2d(sh ? &args.o_s : &args.o_r, ptx::smem_addr(buf),
-                                              col0 / 2, ti.row0 + ti.m_blk * BM + quarter * 32);
+                                              col0 / 2, ti.row0 + wrow0);
                             ptx::bulk_commit();
                         }
                         sbuf ^= 1;
@@ -471,7 +538,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                         __syncwarp();
                         if (lane == 0) {   // columns past n_cols are clipped by the map
                             ptx::tma_store_2d(sh ? &args.o_s : &args.o_r, ptx::smem_addr(buf), col0,
-                                              ti.row0 + ti.m_blk * BM + quarter * 32);
+                                              ti.row0 + wrow0);
                             ptx::bulk_commit();
                         }
                         sbuf ^= 1;
@@ -488,7 +555,12 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&tempty[acc]));
+            if (lane == 0) {
+                if (PAIR && !leader)
+                    ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_addr(&tempty[acc]), 0));
+                else
+                    ptx::mbar_arrive(ptx::smem_addr(&tempty[acc]));
+            }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1;
@@ -500,10 +572,24 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    __syncthreads();   // every role of this CTA has finished
+    if constexpr (PAIR) {
+        // after an abort, loads of the odd CTA that the even one never waited for may still be
+        // landing in this CTA's shared memory: give them time before the pair can exit
+        if (*abort_flag && !leader) {
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 1000000ull) {
+            }
+        }
+        __syncwarp();
+        ptx::cluster_sync();   // neither CTA leaves while the other may still signal it
+    }
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kTmemCols);
+        if constexpr (PAIR)
+            ptx::tmem_dealloc_pair(tmem, kTmemCols);
+        else
+            ptx::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -513,11 +599,55 @@ template <int BN, int STAGES, int EPI, int ABOX = BM>
 cudaError_t launch_tc(const TcArgs& args, int max_tiles, cudaStream_t st) {
     using S = Smem<BN, STAGES, EPI, ABOX>;
     constexpr int EW = epi_warps(EPI);
-    auto kern = gemm_tc_kernel<BN, STAGES, EPI, EW, ABOX>;
+    auto kern = gemm_tc_kernel<BN, STAGES, EPI, EW, ABOX, false>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), S::total);
     if (e != cudaSuccess) return e;
     const int grid = max(1, min(sm_count(), max_tiles));
     e = launch_pdl(kern, dim3(grid), dim3((2 + EW) * 32), S::total, st, args);
+    if (e != cudaSuccess) return e;
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+// CTA-pair launch: clusters of two CTAs, as many clusters as fit on the GPU at once (at most one
+// per 256-row tile), each pair looping over its share of the tiles; max_tiles counts pair tiles.
+template <int BN, int STAGES, int EPI>
+cudaError_t launch_tc_pair(const TcArgs& args, int max_tiles, cudaStream_t st) {
+    using S = Smem<BN, STAGES, EPI, BM, true>;
+    constexpr int EW = epi_warps(EPI);
+    auto kern = gemm_tc_kernel<BN, STAGES, EPI, EW, BM, true>;
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), S::total);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * sm_count());
+    cfg.blockDim = dim3((2 + EW) * 32);
+    cfg.dynamicSmemBytes = S::total;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    // clusters resident at once, per device (a persistent grid larger than that would leave the
+    // last clusters waiting for the first ones to finish all their tiles)
+    static int resident[64] = {0};
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (resident[dev] == 0) {
+        int n = 0;
+        cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
+        if ((e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg)) != cudaSuccess) return e;
+        cfg.numAttrs = 2;
+        if (n <= 0) return cudaErrorLaunchOutOfResources;
+        resident[dev] = n;
+    }
+    cfg.gridDim = dim3(2 * std::max(1, std::min(resident[dev], max_tiles)));
+    e = cudaLaunchKernelEx(&cfg, kern, args);
     if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
@@ -554,16 +684,26 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     const int bn = pick_bn(g.n_routed > 0 ? g.n_cols_r : 0, shared ? g.n_cols_s : 0, EPI);
     // at most 64 tokens: every group (routed or shared) has at most 64 rows
     const bool small_a = EPI != 2 && bn == 256 && g.T_shared > 0 && g.T_shared <= 64;
+    // 256-column tiles of the forward epilogues run as CTA pairs over 256-row tiles when the K
+    // loop is long enough to amortise a pair tile's pipeline start (16+ blocks) and the launch
+    // gains more from the lighter operand feed than it loses to rounding ragged groups up to 256
+    // rows: launches with dense groups only, and the plain epilogue, whose 256-row tiles cost less
+    // than the SwiGLU epilogue's (measured on the expert shapes of the pages' models).
+    const int kb_min = std::min(g.n_routed > 0 ? (int)((g.k_r + BK - 1) / BK) : INT32_MAX,
+                                shared ? (int)((g.k_s + BK - 1) / BK) : INT32_MAX);
+    const bool pair = EPI != 2 && bn == 256 && !small_a && kb_min >= 16 &&
+                      (EPI == 0 || g.n_routed == 0);
     const int a_box = small_a ? 64 : BM;
+    const int b_box = pair ? bn / 2 : bn;
     TcArgs a{};
     if (g.n_routed > 0) {
         if (!encode_bf16_map(&a.a_r, g.a_r, g.a_rows_r, g.k_r, a_box) ||
-            !encode_bf16_map(&a.b_r, g.b_r, g.b_rows_r, g.k_r, bn))
+            !encode_bf16_map(&a.b_r, g.b_r, g.b_rows_r, g.k_r, b_box))
             return cudaErrorInvalidValue;
     }
     if (shared) {
         if (!encode_bf16_map(&a.a_s, g.a_s, g.a_rows_s, g.k_s, a_box) ||
-            !encode_bf16_map(&a.b_s, g.b_s, g.b_rows_s, g.k_s, bn))
+            !encode_bf16_map(&a.b_s, g.b_s, g.b_rows_s, g.k_s, b_box))
             return cudaErrorInvalidValue;
     }
     if (g.n_routed == 0) {   // a dense GEMM: only the shared slot has rows
@@ -619,6 +759,12 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
                            (long)((g.T_shared + BM - 1) / BM) * a.gt.n_tiles_s;
     const int mt = (int)std::min<long>(max_tiles, 1 << 30);
     if constexpr (EPI != 2) {
+        if (pair) {   // tiles of 256 rows: sum over groups of ceil(M_j / 256)
+            const long pr = g.n_routed > 0 ? (long)(g.max_routed_rows / (2 * BM)) + g.n_routed : 0;
+            const long pt = pr * a.gt.n_tiles_r +
+                            (long)((g.T_shared + 2 * BM - 1) / (2 * BM)) * a.gt.n_tiles_s;
+            return launch_tc_pair<256, 6, EPI>(a, (int)std::min<long>(pt, 1 << 30), st);
+        }
         if (small_a) return launch_tc<256, 5, EPI, 64>(a, mt, st);
     }
     if (bn == 256) return launch_tc<256, 4, EPI>(a, mt, st);

@@ -14,14 +14,21 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s: far beyond any legi
 
 // Returns true once the phase with `parity` has completed; false if the CTA is aborting or the
 // wait expired.
+// kCluster: the phase may be completed by arrivals from another CTA of the cluster.
+template <bool kCluster = false>
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+    return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+}
+
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            int* status, uint64_t timeout_ns = kWaitTimeoutNs) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (try_wait<kCluster>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (try_wait<kCluster>(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > timeout_ns) {
             *abort_flag = 1;
@@ -32,10 +39,11 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 }
 
 // Wait used while draining after an abort: bounded, ignores the abort flag.
+template <bool kCluster = false>
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity,
                                            uint64_t timeout_ns = kWaitTimeoutNs) {
     const uint64_t t0 = globaltimer_ns();
-    while (!ptx::mbar_try_wait(bar, parity))
+    while (!try_wait<kCluster>(bar, parity))
         if (globaltimer_ns() - t0 > timeout_ns) return;
 }
 
