@@ -7,7 +7,10 @@
 //
 // The logits of a 128-token tile are one [128 x d] x [d x N'] product: the tile's token rows and
 // the centroids stream through a TMA ring into tcgen05.mma (M = 128, N = N' rounded up to 32),
-// accumulating fp32 logits in TMEM. Four epilogue warps then own one token per thread: each reads
+// accumulating fp32 logits in TMEM. When there are few tiles (decode-sized batches), a cluster of
+// C CTAs shares a tile, each over 1/C of d; the other CTAs leave their partial logits in their
+// shared memory and the first adds them to its own, in rank order, through distributed shared
+// memory, so the sum does not depend on timing. Four epilogue warps then own one token per thread: each reads
 // its logit row from TMEM once (warp w sees TMEM lanes 32*(w%4) .. +31), adds the optional bias,
 // keeps the row in the (by then idle) TMA ring, and computes the softmax, a register top-K'
 // (ranked by logit; the lower index wins ties), the gates, the tile's expert histogram and, by a
@@ -33,6 +36,7 @@ struct RouterArgs {
     CUtensorMap b;        // centroids [N', d], box [n_pad x 64]
     const float* bias;    // [N'] or null
     int T, N, K, renorm, skip, k_blocks, n_pad, stages, tmem_cols;
+    int csize;            // CTAs per tile (cluster size); CTA r takes K blocks [r kb/C, (r+1) kb/C)
     uint32_t stage_bytes;
     int* topk_idx;
     float* topk_gate;
@@ -204,6 +208,8 @@ __device__ __forceinline__ void route_tile(const RouterArgs& a, uint32_t tmem_la
     const int t = tile * RBM + row;
     const bool valid = t < a.T;
     const int n_chunks = a.n_pad / 32;
+    // the other CTAs of the cluster keep their partial logits at the same offset as zc
+    const uint32_t part = ptx::smem_addr(zc);
     // pass 1 (TMEM): biased logits, their maximum and the top list
     float zmax = -INFINITY;
     TopK<KMAX> top;
@@ -212,6 +218,15 @@ __device__ __forceinline__ void route_tile(const RouterArgs& a, uint32_t tmem_la
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(tmem_lanes + c * 32, v);
         ptx::tmem_ld_wait();
+        for (int r = 1; r < a.csize; ++r) {   // partial sums of the later K slices, in rank order
+            const uint32_t peer = ptx::mapa(part, (uint32_t)r);
+            float pv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                pv[i] = ptx::ld_cluster_f32(peer + (uint32_t)(((c * 32 + i) * RBM + row) * 4));
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + pv[i]);
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int j = c * 32 + i;
@@ -381,7 +396,12 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     int* chosen = reinterpret_cast<int*>(aux_s + kMaxRouted);     // [128][kMaxTopK]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x;
+    const int crank = a.csize > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const bool leader = crank == 0;
+    const int tile = blockIdx.x / a.csize;
+    const int n_tiles = gridDim.x / a.csize;
+    const int kb_begin = crank * a.k_blocks / a.csize;
+    const int kb_end = (crank + 1) * a.k_blocks / a.csize;
     const int N = a.N;
 
     if (threadIdx.x == 0) {
@@ -432,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int kb = 0; kb < a.k_blocks; ++kb) {
+            for (int kb = kb_begin; kb < kb_end; ++kb) {
                 if (!wait_phase(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag, a.status)) {
                     ok = false;
                     break;
@@ -465,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true, any = false;
-            for (int kb = 0; kb < a.k_blocks; ++kb) {
+            for (int kb = kb_begin; kb < kb_end; ++kb) {
                 if (!wait_phase(ptx::smem_addr(&full[stage]), phase, abort_flag, a.status)) {
                     ok = false;
                     break;
@@ -477,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
                 for (int k = 0; k < RBK / 16; ++k)
                     ptx::mma_f16(tmem, ptx::sw128_kmajor_desc(a0 + k * 32),
                                  ptx::sw128_kmajor_desc(b0 + k * 32), idesc,
-                                 (kb | k) != 0 ? 1u : 0u);
+                                 (kb != kb_begin || k != 0) ? 1u : 0u);
                 any = true;
                 ptx::mma_commit(ptx::smem_addr(&empty[stage]));
                 if (++stage == a.stages) {
@@ -491,7 +511,32 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
                 drain_wait(ptx::smem_addr(drain), 0);
             }
         }
-    } else {
+    } else if (!leader) {
+        // ------------------------------------------- partial logits of a later K slice ----
+        // kept in the idle ring as [n_pad][128] floats for the first CTA of the cluster
+        const int quarter = warp & 3;
+        int ok = 1;
+        if (lane == 0) ok = wait_phase(ptx::smem_addr(tfull), 0, abort_flag, a.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        float* part = reinterpret_cast<float*>(base);
+        const int row = quarter * 32 + lane;
+        if (ok) ptx::tc_fence_after();
+        for (int c = 0; c < a.n_pad / 32; ++c) {
+            uint32_t v[32];
+            if (ok) {
+                ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
+                ptx::tmem_ld_wait();
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i)   // zeros if this CTA gave up (its status is set)
+                part[(c * 32 + i) * RBM + row] = ok ? __uint_as_float(v[i]) : 0.f;
+        }
+    }
+    if (a.csize > 1) {   // the partial logits are in place; every thread of the cluster
+        __syncwarp();
+        ptx::cluster_sync();
+    }
+    if (warp >= 2 && leader) {
         // --------------------------------------------------------------------- epilogue ----
         const int quarter = warp & 3;
         const int et = threadIdx.x - 64;   // 0..127 over the four epilogue warps
@@ -514,7 +559,6 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
         ptx::tc_fence_before();
         epilogue_bar();
         if (routed_here) {
-            const int n_tiles = gridDim.x;
             for (int j = et; j < N; j += 128) {
                 const float col = ((colsum[j] + colsum[kMaxRouted + j]) +
                                    colsum[2 * kMaxRouted + j]) + colsum[3 * kMaxRouted + j];
@@ -533,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
 
     ptx::tc_fence_before();
     __syncthreads();
+    if (a.csize > 1) ptx::cluster_sync();   // the first CTA has read the others' partial logits
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, a.tmem_cols);
@@ -560,6 +605,12 @@ static cudaError_t router_args(const Dims& m, const void* u, const void* centroi
     int cols = 32;
     while (cols < a.n_pad) cols *= 2;
     a.tmem_cols = cols;
+    // few tiles: up to 8 CTAs per tile, while the grid stays within one wave and every CTA keeps
+    // at least two K blocks
+    const int n_tiles = (m.T + RBM - 1) / RBM;
+    int c = 1;
+    while (c < 8 && (long)n_tiles * c * 2 <= sm_count() && a.k_blocks / (c * 2) >= 2) c *= 2;
+    a.csize = c;
     return cudaSuccess;
 }
 
@@ -571,7 +622,25 @@ static cudaError_t launch_router_kernel(const Dims& m, const RouterArgs& a, cuda
     auto kern = router_tc_kernel<KMAX, BWD>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3(n_tiles), dim3(kThreads), smem, st, a);
+    if (a.csize == 1) {
+        e = launch_pdl(kern, dim3(n_tiles), dim3(kThreads), smem, st, a);
+    } else {   // clusters of csize CTAs per tile
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(n_tiles * a.csize);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)a.csize;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, kern, a);
+    }
     if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();
@@ -615,6 +684,7 @@ cudaError_t launch_router_bwd(const Dims& m, const void* u, const void* centroid
     cudaError_t e = router_args(m, u, centroids, bias, a);
     if (e != cudaSuccess) return e;
     a.topk_idx = const_cast<int*>(topk_idx);
+    a.csize = 1;   // the backward epilogue needs the whole logit row of a token in one CTA
     a.dgate = dgate;
     a.counts = counts;
     a.dz = static_cast<__nv_bfloat16*>(dz);
