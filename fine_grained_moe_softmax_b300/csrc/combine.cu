@@ -172,8 +172,11 @@ cudaError_t launch_combine(const Dims& m, const void* u, const void* y_r, const 
         else combine_t<float, 16>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
     } else {
         using B = __nv_bfloat16;
+        // the fine-grained configurations' K' (6, 12) get exact slot counts: no dummy row loads
         if (m.K <= 4) combine_t<B, 4>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
+        else if (m.K <= 6) combine_t<B, 6>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
         else if (m.K <= 8) combine_t<B, 8>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
+        else if (m.K <= 12) combine_t<B, 12>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
         else combine_t<B, 16>(m, u, y_r, y_s, perm_slot, gate, h, status, st, row_limit);
     }
     note_launches(1);
