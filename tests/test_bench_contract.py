@@ -59,3 +59,22 @@ def test_our_arm_line_matches_the_reference_arm():
     ref = _bench("--impl", "reference", "--config", "2b_bf16", "--steps", "1", "--warmup", "3")
     for k in ("metric", "unit", "higher_is_better", "config"):
         assert ours[k] == ref[k], k
+
+
+def test_roofline_inputs_of_the_routed_gate_up_launch():
+    """The roofline describes one gate/up launch: over the routed groups only when the shared
+    group has a launch of its own, over every group otherwise."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import moe_inputs
+    sh = moe_inputs.CONFIGS["16b_bf16"]
+    T = sh.T
+    routed = 4.0 * sh.d * sh.inter * T * sh.top_k
+    assert bench.gate_up_flops(sh, T, with_shared=False) == routed
+    assert bench.gate_up_flops(sh, T) == routed * (sh.top_k + sh.n_shared) / sh.top_k
+    every_expert = [1] * sh.n_routed
+    # routed weights + permuted rows read, activations written (bf16)
+    want = (sh.n_routed * 2 * sh.inter * sh.d + T * sh.top_k * sh.d + T * sh.top_k * sh.inter) * 2
+    assert bench.gate_up_bytes(sh, T, every_expert, with_shared=False) == want
+    assert bench.gate_up_traffic("16b_bf16", "gemm_gate_up_routed") == 1141014016 + 259321856
+    assert bench.gate_up_traffic("2b_bf16", "gemm_gate_up_routed") is None
