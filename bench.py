@@ -97,6 +97,24 @@ def load_peaks():
     return 6400.0, 1800.0, 1400.0, "fallback"
 
 
+def layer_roofline(sh, T, counts, hbm_gbs, bf16_tf) -> dict:
+    """Roofline of one layer call: the slower of its algorithmic FLOPs at the bf16 peak and its
+    algorithmic bytes at the HBM copy bandwidth. The bytes are the weights it must read (shared
+    experts, centroids, and every routed expert that received a token), u in, h out, and the
+    routing outputs (indices and gates)."""
+    es = 4 if sh.dtype == "f32" else 2
+    touched = int(sum(1 for c in counts if c > 0))
+    shared = 0 if sh.drop_shared else sh.n_shared
+    weights = (shared + touched) * 3 * sh.inter * sh.d * es + sh.n_routed * sh.d * es
+    acts = 2 * T * sh.d * es + T * sh.top_k * 8
+    flops = flops_per_token(sh) * T
+    t_flop = flops / (bf16_tf * 1e12)
+    t_bytes = (weights + acts) / (hbm_gbs * 1e9)
+    return {"bound": "tensor" if t_flop >= t_bytes else "hbm",
+            "roofline_ms": 1e3 * max(t_flop, t_bytes), "flops": flops,
+            "bytes": float(weights + acts)}
+
+
 def rank_token_seed(sh, rank: int) -> int:
     """Each rank draws its own token batch; the expert weights are the same on every rank."""
     return sh.seed + 7919 * rank
@@ -349,36 +367,11 @@ def run_ours(args, sh, rank, world, local_rank):
         return
 
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = load_peaks()
-    # the dominant launch: the gate/up GEMM over the routed groups (over every group when the
-    # shared group was not split off into a launch of its own)
-    split = n_split > 0
-    if n_split not in (0, n_prof):
-        raise RuntimeError(f"{n_split} of {n_prof} profiled calls split the gate/up GEMM")
-    traffic = gate_up_traffic(sh.name, "gemm_gate_up_routed" if split else "gemm_gate_up")
     counts_host = layer.counts.cpu().tolist()
     tokens = T * world * args.steps
     value = tokens / (total_ms / 1e3)
     e2e_value = tokens / (e2e_ms / 1e3)
-    gu_ms = gu_launch_ms / max(n_prof, 1)
-    gu_flops = gate_up_flops(sh, T, with_shared=not split)
-    gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
-    # the launch is bound by whichever of its FLOPs and its algorithmic bytes takes longer at peak
-    gu_bytes = gate_up_bytes(sh, T, counts_host, with_shared=not split)
-    hbm_bound = gu_bytes / (hbm_gbs * 1e9) > gu_flops / (bf16_tf * 1e12)
-    gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
-    kernel = "gemm_tc_kernel (gate/up + SwiGLU epilogue, " + \
-        ("routed groups; the shared group runs in a launch of its own)" if split else "all groups)")
-    if hbm_bound:
-        roof = {"bound": "hbm", "kernel": kernel,
-                "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
-                "traffic": traffic, "peak_source": f"{peak_src} HBM copy",
-                "algorithmic_bytes": gu_bytes}
-    else:
-        roof = {"bound": "tensor", "kernel": kernel,
-                "achieved": gu_tflops, "peak": bf16_tf, "unit": "TFLOP/s",
-                "frac": gu_tflops / bf16_tf, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 burst"}
-    roof["launch_ms"] = gu_ms
+    roof = dominant_roofline(sh, T, counts_host, gu_launch_ms, n_prof, n_split)
     layer_tflops = flops_per_token(sh) * T / (total_ms / args.steps / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -396,6 +389,18 @@ def run_ours(args, sh, rank, world, local_rank):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    lr = layer_roofline(sh, T, counts_host, hbm_gbs, bf16_tf)
+    line["layer_roofline"].update({"bound": lr["bound"], "roofline_ms": lr["roofline_ms"],
+                                   "frac": lr["roofline_ms"] / (total_ms / args.steps)})
+    if world == 1 and not args.no_per_config and args.tokens is None and not args.graph \
+            and sh.name == "16b_bf16":
+        del layer, graph, flush
+        torch.cuda.empty_cache()
+        pc_clocks = ClockSampler(local_rank)
+        pc_clocks.start()
+        time.sleep(0.3)
+        runs = [measure_workload(name, g, args.per_config_steps, 3, dev) for name, g in PER_CONFIG]
+        line["per_config"] = {"runs": runs, "clocks": pc_clocks.stop()}
     if world == 1 and not args.no_cpu_baseline:
         n = args.cpu_tokens
         rate, secs, threads = oracle_sample_rate(sh, n)
@@ -403,6 +408,112 @@ def run_ours(args, sh, rank, world, local_rank):
                                 "sample": f"{n} tokens of the {sh.name} workload, fp64 oracle, "
                                           f"{secs:.1f} s"}
     print(json.dumps(line), flush=True)
+
+
+def dominant_roofline(sh, T, counts, gu_launch_ms, n_prof, n_split) -> dict:
+    """`roofline` of the dominant launch, the gate/up GEMM over the routed groups (over every
+    group when the shared group was not split off into a launch of its own), from its summed
+    CUDA-event time over n_prof profiled calls. Bound: whichever of its FLOPs at the bf16 peak
+    and its algorithmic bytes at the HBM copy bandwidth takes longer."""
+    hbm_gbs, bf16_tf, _, peak_src = load_peaks()
+    split = n_split > 0
+    if n_split not in (0, n_prof):
+        raise RuntimeError(f"{n_split} of {n_prof} profiled calls split the gate/up GEMM")
+    kname = "gemm_gate_up_routed" if split else "gemm_gate_up"
+    traffic = gate_up_traffic(sh.name, kname)
+    gu_ms = gu_launch_ms / max(n_prof, 1)
+    gu_flops = gate_up_flops(sh, T, with_shared=not split)
+    gu_tflops = gu_flops / (gu_ms / 1e3) / 1e12
+    gu_bytes = gate_up_bytes(sh, T, counts, with_shared=not split)
+    hbm_bound = gu_bytes / (hbm_gbs * 1e9) > gu_flops / (bf16_tf * 1e12)
+    gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
+    kernel = "gemm_tc_kernel (gate/up + SwiGLU epilogue, " + \
+        ("routed groups; the shared group runs in a launch of its own)" if split else "all groups)")
+    if hbm_bound:
+        roof = {"bound": "hbm", "kernel": kernel,
+                "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
+                "traffic": traffic, "peak_source": f"{peak_src} HBM copy",
+                "algorithmic_bytes": gu_bytes}
+    else:
+        roof = {"bound": "tensor", "kernel": kernel,
+                "achieved": gu_tflops, "peak": bf16_tf, "unit": "TFLOP/s",
+                "frac": gu_tflops / bf16_tf, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst"}
+    roof["traffic_source"] = (
+        "profiles/gemm_traffic_full_size.txt: dram__bytes_read.sum + dram__bytes_write.sum of "
+        f"this launch ({kname}) from an earlier one-pass ncu capture at full size, not this run"
+        if traffic is not None else "not captured for this workload")
+    roof["launch_ms"] = gu_ms
+    return roof
+
+
+# Workloads timed beside the headline in the default run: (name, CUDA-graph replay).
+PER_CONFIG = [("2b_bf16", False), ("145b_zipf_bf16", False), ("16b_decode_bf16", False),
+              ("16b_decode_bf16", True)]
+
+
+def measure_workload(name, graph, steps, warmup, dev) -> dict:
+    """ms per layer call of one more workload on this GPU (L2 flushed between steps, CUDA events
+    on the launching stream), its layer roofline fraction and its dominant launch's fraction."""
+    import torch
+
+    import fine_grained_moe_softmax_b300 as moe
+    sh = moe_inputs.CONFIGS[name]
+    T = sh.T
+    inputs = moe_inputs.make_inputs(sh)
+    layer = moe.MoELayer(moe.MoEConfig.from_shape(sh), inputs["centroids"], inputs["w_gate"],
+                         inputs["w_up"], inputs["w_down"], inputs["bias"], device=dev)
+    u = inputs["u"].to(dev)
+    del inputs
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        layer.forward(u)
+    torch.cuda.synchronize(dev)
+    if layer.device_status() != 0:
+        raise RuntimeError(f"{name}: device status after warm-up")
+    g = layer.capture(u)[0] if graph else None
+    if g is not None:
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        if g is not None:
+            g.replay()
+        else:
+            layer.forward(u)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+    moe.moe_profile_enable(True, steps)
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        layer.forward(u)
+    torch.cuda.synchronize(dev)
+    stage_ms, n_prof = moe.moe_profile_read()
+    gu_launch_ms, _, n_split = moe.moe_profile_read_gate_up()
+    moe.moe_profile_enable(False)
+    if layer.device_status() != 0:
+        raise RuntimeError(f"{name}: device status after timing")
+    counts = layer.counts.cpu().tolist()
+    hbm_gbs, bf16_tf, _, _ = load_peaks()
+    lr = layer_roofline(sh, T, counts, hbm_gbs, bf16_tf)
+    out = {"workload": name, "T": T,
+           "launch": "CUDA graph replay of moe_layer_forward" if graph
+                     else "direct moe_layer_forward calls",
+           "steps": steps, "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3),
+           "layer_roofline": {"bound": lr["bound"], "roofline_ms": lr["roofline_ms"],
+                              "frac": lr["roofline_ms"] / ms},
+           "dominant_launch": dominant_roofline(sh, T, counts, gu_launch_ms, n_prof, n_split),
+           "stage_ms_per_step (direct calls)": {k: v / max(n_prof, 1)
+                                                for k, v in stage_ms.items()}}
+    del layer, g, flush, u
+    torch.cuda.empty_cache()
+    return out
 
 
 def backward_flops_per_token(sh) -> float:
@@ -500,6 +611,9 @@ def main():
                     help="time the layer backward instead of the forward (1 GPU)")
     ap.add_argument("--graph", action="store_true",
                     help="time CUDA-graph replays of the layer call instead of direct calls")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads timed beside the 16B-like headline")
+    ap.add_argument("--per-config-steps", type=int, default=10)
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (small profiling captures only; not a bench line)")
     args = ap.parse_args()

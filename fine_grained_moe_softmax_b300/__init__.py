@@ -8,6 +8,7 @@ from .binding import (MOE_DTYPE_BF16, MOE_DTYPE_F32, N_STAGES, STAGE_NAMES, MoEC
                       moe_backward_workspace_bytes, moe_balance_stats, moe_combine,
                       moe_device_status, moe_expert_ffn, moe_launch_count, moe_layer_backward,
                       moe_layer_backward_saved, moe_layer_forward, moe_layer_forward_train,
+                      moe_layer_routing,
                       moe_pack_weights, moe_pack_weights_backward, moe_packed_backward_bytes,
                       moe_packed_weight_bytes, moe_permute, moe_profile_enable, moe_profile_read,
                       moe_profile_read_gate_up,
@@ -19,6 +20,7 @@ __all__ = ["MOE_DTYPE_BF16", "MOE_DTYPE_F32", "N_STAGES", "STAGE_NAMES", "MoECon
            "MoELayer", "moe_backward_workspace_bytes", "moe_balance_stats", "moe_combine",
            "moe_device_status", "moe_expert_ffn", "moe_launch_count", "moe_layer_backward",
            "moe_layer_backward_saved", "moe_layer_forward", "moe_layer_forward_train",
+           "moe_layer_routing",
            "moe_pack_weights", "moe_pack_weights_backward", "moe_packed_backward_bytes",
            "moe_packed_weight_bytes", "moe_permute", "moe_profile_enable", "moe_profile_read",
            "moe_profile_read_gate_up",

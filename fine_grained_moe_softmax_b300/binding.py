@@ -61,6 +61,9 @@ _SIG = {
     "moe_balance_stats": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_layer_forward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                          ctypes.c_size_t, _P]),
+    "moe_layer_routing": (ctypes.c_int, [_CFG, _P, ctypes.c_size_t, ctypes.POINTER(_P),
+                                         ctypes.POINTER(_P), ctypes.POINTER(_P),
+                                         ctypes.POINTER(_P)]),
     "moe_backward_workspace_bytes": (ctypes.c_size_t, [_CFG]),
     "moe_packed_backward_bytes": (ctypes.c_size_t, [_CFG]),
     "moe_pack_weights_backward": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P]),
@@ -184,6 +187,24 @@ def moe_layer_forward(cfg, u, centroids, logit_bias, packed_w, h, topk_idx, topk
                                    _ptr(packed_w), _ptr(h), _ptr(topk_idx), _ptr(topk_gate),
                                    _ptr(counts), _ptr(f), _ptr(P), _ptr(losses), _ptr(ws),
                                    _nbytes(ws), _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_routing(cfg, ws) -> dict:
+    """Views into ``ws`` of the routing tables the last moe_layer_forward on it left there:
+    offsets [N'+1], perm_token [T*K'], perm_slot [T*K'] (int32) and psum [N'] (fp32)."""
+    ptrs = [ctypes.c_void_p() for _ in range(4)]
+    _check(lib().moe_layer_routing(ctypes.byref(cfg), _ptr(ws), _nbytes(ws),
+                                   *[ctypes.byref(p) for p in ptrs]), "moe_layer_routing")
+    base = ws.data_ptr()
+    TK, N = cfg.T * cfg.top_k, cfg.n_routed
+    out = {}
+    for name, p, n, dt in (("offsets", ptrs[0], N + 1, torch.int32),
+                           ("perm_token", ptrs[1], TK, torch.int32),
+                           ("perm_slot", ptrs[2], TK, torch.int32),
+                           ("psum", ptrs[3], N, torch.float32)):
+        off = p.value - base
+        out[name] = ws[off:off + 4 * n].view(dt)
+    return out
 
 
 def moe_backward_workspace_bytes(cfg: MoEConfig) -> int:

@@ -12,22 +12,9 @@ namespace moe {
 namespace {
 
 int check_bwd(const moe_config* c, Dims* m) {
-    if (!c) return MOE_ERR_INVALID_ARG;
-    const size_t ws = moe_workspace_bytes(c);   // 0 exactly for configurations rejected elsewhere
-    if (ws == 0) {
-        const bool invalid = c->T < 0 || c->d <= 0 || c->n_shared < 0 || c->n_routed <= 0 ||
-                             c->inter <= 0 || c->top_k <= 0 || c->top_k > c->n_routed ||
-                             c->n_groups <= 0 || c->n_groups > c->n_routed ||
-                             (c->renormalize != 0 && c->renormalize != 1) ||
-                             (c->dtype != MOE_DTYPE_F32 && c->dtype != MOE_DTYPE_BF16) ||
-                             c->skip_top < 0 || c->skip_top + c->top_k > c->n_routed ||
-                             (c->drop_shared != 0 && c->drop_shared != 1);
-        return invalid ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
-    }
-    if (c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
-    *m = Dims{c->T, c->d, c->n_shared, c->n_routed, c->inter, c->top_k, c->renormalize,
-              c->n_groups, c->alpha1, c->alpha2, c->dtype, c->skip_top, c->drop_shared};
-    return MOE_OK;
+    const int rc = validate_config(c, m);
+    if (rc != MOE_OK) return rc;
+    return c->dtype == MOE_DTYPE_BF16 ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }

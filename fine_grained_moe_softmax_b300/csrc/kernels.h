@@ -11,6 +11,11 @@
 
 namespace moe {
 
+// Checks a caller configuration against the rules every entry point applies (null, negative or
+// inconsistent fields: MOE_ERR_INVALID_ARG; valid but outside this build's shapes:
+// MOE_ERR_UNSUPPORTED) and fills *m on MOE_OK (moe_api.cu).
+int validate_config(const moe_config* c, Dims* m);
+
 // Router: per 128-token tile, logits, softmax, top-k, gates, tile histogram and affinity sums
 // (tables expert-major: [N][n_tiles]).
 cudaError_t launch_router(const Dims& m, const void* u, const void* centroids, const float* bias,

@@ -78,9 +78,8 @@ cudaError_t ensure_smem(const void* func, size_t bytes) {
     return e;
 }
 
-namespace {
-
-int check_cfg(const moe_config* c, Dims* m) {
+// The configuration rules of every entry point (include/moe_b300.h, "Supported shapes").
+int validate_config(const moe_config* c, Dims* m) {
     if (!c) return MOE_ERR_INVALID_ARG;
     if (c->T < 0 || c->d <= 0 || c->n_shared < 0 || c->n_routed <= 0 || c->inter <= 0 ||
         c->top_k <= 0 || c->top_k > c->n_routed || c->n_groups <= 0 ||
@@ -112,6 +111,8 @@ int check_cfg(const moe_config* c, Dims* m) {
     m->drop_shared = c->drop_shared;
     return MOE_OK;
 }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -178,20 +179,20 @@ extern "C" {
 
 size_t moe_workspace_bytes(const moe_config* cfg) {
     Dims m;
-    if (check_cfg(cfg, &m) != MOE_OK) return 0;
+    if (validate_config(cfg, &m) != MOE_OK) return 0;
     return ws_layout(m).total;
 }
 
 size_t moe_packed_weight_bytes(const moe_config* cfg) {
     Dims m;
-    if (check_cfg(cfg, &m) != MOE_OK) return 0;
+    if (validate_config(cfg, &m) != MOE_OK) return 0;
     return pack_layout(m).total * (size_t)m.elem();
 }
 
 int moe_pack_weights(const moe_config* cfg, const void* w_gate, const void* w_up,
                      const void* w_down, void* packed, moe_stream_t stream) {
     Dims m;
-    int rc = check_cfg(cfg, &m);
+    int rc = validate_config(cfg, &m);
     if (rc != MOE_OK) return rc;
     if (!w_gate || !w_up || !w_down || !packed || !aligned16(w_gate) || !aligned16(w_up) ||
         !aligned16(w_down) || !aligned16(packed))
@@ -203,7 +204,7 @@ int moe_route(const moe_config* cfg, const void* u, const void* centroids,
               const float* logit_bias, int32_t* topk_idx, float* topk_gate, int32_t* counts,
               float* psum, void* ws, size_t ws_bytes, moe_stream_t stream) {
     Dims m;
-    int rc = check_cfg(cfg, &m);
+    int rc = validate_config(cfg, &m);
     if (rc != MOE_OK) return rc;
     if ((m.T > 0 && (!u || !topk_idx || !topk_gate || !aligned16(u))) || !centroids ||
         !aligned16(centroids) || !counts || !psum)
@@ -234,7 +235,7 @@ int moe_permute(const moe_config* cfg, const int32_t* topk_idx, const int32_t* c
                 int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, void* ws,
                 size_t ws_bytes, moe_stream_t stream) {
     Dims m;
-    int rc = check_cfg(cfg, &m);
+    int rc = validate_config(cfg, &m);
     if (rc != MOE_OK) return rc;
     if ((m.T > 0 && (!topk_idx || !perm_token || !perm_slot)) || !offsets)
         return MOE_ERR_INVALID_ARG;
@@ -266,7 +267,7 @@ int moe_expert_ffn(const moe_config* cfg, const void* u, const void* packed_w,
                    const int32_t* offsets, const int32_t* perm_token, void* y_routed,
                    void* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
     Dims m;
-    int rc = check_cfg(cfg, &m);
+    int rc = validate_config(cfg, &m);
     if (rc != MOE_OK) return rc;
     if (!packed_w || !aligned16(packed_w) || !offsets ||
         (m.T > 0 && (!u || !aligned16(u) || !perm_token || !y_routed || !aligned16(y_routed) ||
@@ -290,7 +291,7 @@ int moe_combine(const moe_config* cfg, const void* u, const void* y_routed, cons
                 const int32_t* perm_slot, const float* topk_gate, void* h, void* ws,
                 size_t ws_bytes, moe_stream_t stream) {
     Dims m;
-    int rc = check_cfg(cfg, &m);
+    int rc = validate_config(cfg, &m);
     if (rc != MOE_OK) return rc;
     if (m.T > 0 && (!u || !y_routed || !perm_slot || !topk_gate || !h || !aligned16(u) ||
                     !aligned16(y_routed) || !aligned16(h) || (m.shared_active() && !y_shared) ||
@@ -307,7 +308,7 @@ int moe_combine(const moe_config* cfg, const void* u, const void* y_routed, cons
 int moe_balance_stats(const moe_config* cfg, const int32_t* counts, const float* psum, float* f,
                       float* P, float* losses, moe_stream_t stream) {
     Dims m;
-    int rc = check_cfg(cfg, &m);
+    int rc = validate_config(cfg, &m);
     if (rc != MOE_OK) return rc;
     if (!counts || !psum || !f || !P || !losses) return MOE_ERR_INVALID_ARG;
     return cuda_rc(launch_balance(m, counts, psum, f, P, losses, (cudaStream_t)stream));
@@ -318,7 +319,7 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
                       float* topk_gate, int32_t* counts, float* f, float* P, float* losses,
                       void* ws, size_t ws_bytes, moe_stream_t stream) {
     Dims m;
-    int rc = check_cfg(cfg, &m);
+    int rc = validate_config(cfg, &m);
     if (rc != MOE_OK) return rc;
     if ((m.T > 0 && (!u || !h || !topk_idx || !topk_gate || !aligned16(u) || !aligned16(h))) ||
         !centroids || !aligned16(centroids) || !packed_w || !aligned16(packed_w) || !counts ||
@@ -408,6 +409,22 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
     mk.mark(6);   // the statistics were produced by the finalize kernel of the permute stage
     mk.mark(7);
     return cuda_rc(e);
+}
+
+int moe_layer_routing(const moe_config* cfg, const void* ws, size_t ws_bytes,
+                      const int32_t** offsets, const int32_t** perm_token,
+                      const int32_t** perm_slot, const float** psum) {
+    Dims m;
+    int rc = validate_config(cfg, &m);
+    if (rc != MOE_OK) return rc;
+    if ((rc = check_ws(m, ws, ws_bytes)) != MOE_OK) return rc;
+    const WsLayout L = ws_layout(m);
+    void* w = const_cast<void*>(ws);
+    if (offsets) *offsets = at<int>(w, L.offsets);
+    if (perm_token) *perm_token = at<int>(w, L.perm_token);
+    if (perm_slot) *perm_slot = at<int>(w, L.perm_slot);
+    if (psum) *psum = at<float>(w, L.psum);
+    return MOE_OK;
 }
 
 int moe_device_status(const void* ws, moe_stream_t stream) {

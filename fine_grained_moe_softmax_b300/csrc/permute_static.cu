@@ -24,7 +24,10 @@ constexpr size_t kStaticScratchBytes = 2 * kStaticTileEntries * sizeof(int);
 __device__ __align__(256) unsigned char g_permute_scratch[kStaticScratchBytes];
 
 // Device address of g_permute_scratch for each device, looked up once with that device current.
-// In host code the array's name is only a host-side stand-in, so kernels get this address.
+// In host code the array's name is only a host-side stand-in, so kernels get this address. The
+// cached address stays valid as long as the device's primary context does: a cudaDeviceReset
+// while the library is loaded would leave it stale, so callers of moe_permute_static must not
+// reset the device in between.
 constexpr int kMaxDevices = 64;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
 std::mutex g_scratch_mu;
@@ -54,24 +57,11 @@ using namespace moe;
 extern "C" int moe_permute_static(const moe_config* cfg, const int32_t* topk_idx,
                                   const int32_t* counts, int32_t* offsets, int32_t* perm_token,
                                   int32_t* perm_slot, int32_t* status, moe_stream_t stream) {
-    if (!cfg) return MOE_ERR_INVALID_ARG;
-    const moe_config c = *cfg;
-    // the same configuration rules as every other entry point: moe_workspace_bytes() returns 0
-    // exactly for the configurations they reject
-    if (moe_workspace_bytes(&c) == 0) {
-        const bool invalid = c.T < 0 || c.d <= 0 || c.n_shared < 0 || c.n_routed <= 0 ||
-                             c.inter <= 0 || c.top_k <= 0 || c.top_k > c.n_routed ||
-                             c.n_groups <= 0 || c.n_groups > c.n_routed ||
-                             (c.renormalize != 0 && c.renormalize != 1) ||
-                             (c.dtype != MOE_DTYPE_F32 && c.dtype != MOE_DTYPE_BF16) ||
-                             c.skip_top < 0 || c.skip_top + c.top_k > c.n_routed ||
-                             (c.drop_shared != 0 && c.drop_shared != 1);
-        return invalid ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
-    }
-    if ((c.T > 0 && (!topk_idx || !perm_token || !perm_slot)) || !offsets)
+    Dims m;
+    const int rc = validate_config(cfg, &m);   // the rules of every other entry point
+    if (rc != MOE_OK) return rc;
+    if ((m.T > 0 && (!topk_idx || !perm_token || !perm_slot)) || !offsets)
         return MOE_ERR_INVALID_ARG;
-    Dims m{c.T, c.d, c.n_shared, c.n_routed, c.inter, c.top_k, c.renormalize, c.n_groups,
-           c.alpha1, c.alpha2, c.dtype, c.skip_top, c.drop_shared};
     const size_t n_tiles = ((size_t)m.T + kRouteTile - 1) / kRouteTile;
     if (n_tiles * (size_t)m.N > kStaticTileEntries) return MOE_ERR_UNSUPPORTED;
     void* scratch = nullptr;

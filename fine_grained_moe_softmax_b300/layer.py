@@ -144,18 +144,31 @@ class MoELayer:
             self.forward(u)
         return graph, B.moe_launch_count() - n0
 
+    def routing(self, T: Optional[int] = None) -> dict:
+        """The routing tables of the last ``forward`` on T tokens (default: the layer's T), as
+        views into the workspace (moe_layer_routing): offsets, perm_token, perm_slot, psum.
+        They are overwritten by the next call."""
+        return B.moe_layer_routing(self.cfg_for(self.cfg.T if T is None else T), self.ws)
+
     def device_status(self, stream=None) -> int:
         return B.moe_device_status(self.ws, stream)
 
-    def global_balance_stats(self, T_local: int, group=None, stream=None):
-        """Balance statistics over the tokens of every rank in ``group``: the per-rank counts and
-        affinity sums (2N' values) are summed across ranks, then moe_balance_stats runs with the
-        global token count. Returns (f, P, losses) device tensors. Only needed when the token
-        batch is split across GPUs; a single GPU's forward already fills f, P and losses.
-        The local affinity sums are recovered as P * T_local (within an fp32 rounding)."""
+    def global_balance_stats(self, T_local: int, group=None, stream=None, via_host=False):
+        """Balance statistics over the tokens of every rank in ``group`` after a ``forward`` on
+        T_local tokens: the per-rank selection counts and affinity sums (2N' values, the raw sums
+        the forward left in its workspace) are summed across ranks, then moe_balance_stats runs
+        with the global token count. Returns (f, P, losses) device tensors. Only needed when the
+        token batch is split across GPUs; a single GPU's forward already fills f, P and losses.
+        ``via_host`` all-reduces CPU copies (for a gloo group)."""
         counts = self.counts.clone()
-        psum = self.P * float(T_local)
-        T_total = allreduce_routing_stats(counts, psum, T_local, group)
+        psum = self.routing(T_local)["psum"].clone()
+        if via_host:
+            c_h, p_h = counts.cpu(), psum.cpu()
+            T_total = allreduce_routing_stats(c_h, p_h, T_local, group)
+            counts.copy_(c_h)
+            psum.copy_(p_h)
+        else:
+            T_total = allreduce_routing_stats(counts, psum, T_local, group)
         cfg = copy.copy(self.cfg)
         cfg.T = T_total
         f = torch.empty_like(self.f)

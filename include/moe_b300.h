@@ -148,6 +148,19 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
                       float* topk_gate, int32_t* counts, float* f, float* P, float* losses,
                       void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* The routing tables that the last moe_layer_forward on `ws` left in its workspace, as device
+ * pointers into ws: offsets [N'+1], perm_token [T*K'] and perm_slot [T*K'] (the dispatch
+ * permutation, as moe_permute returns it) and psum [N'] (sum over the call's tokens of s_{t,j},
+ * as moe_route returns it; the raw sums behind P, which token-sharded callers add up across
+ * ranks before moe_balance_stats). cfg must be that call's configuration (same T) and ws_bytes
+ * at least moe_workspace_bytes(cfg). The pointers are valid once that call has completed on its
+ * stream and until the next call that uses ws; they are read-only. Any output may be NULL.
+ * Launches nothing and does not synchronise. [P2 §2.3: P_i from the affinity sums; P1 §方法细节:
+ * the chosen experts' rows] */
+int moe_layer_routing(const moe_config* cfg, const void* ws, size_t ws_bytes,
+                      const int32_t** offsets, const int32_t** perm_token,
+                      const int32_t** perm_slot, const float** psum);
+
 /* ---- backward (training) ---- */
 
 /* The gradients of the training objective  sum_t dh_t . h_t + L_ExpBal + L_DevBal  with respect to
@@ -213,8 +226,10 @@ const char* moe_status_string(int status);
  * Scratch: a fixed 1 MiB array inside this library, held on every GPU that loads the library until
  * the process exits. Limit: ceil(T / 128) * N' <= 131072 (for example T <= 65536 at N' = 256,
  * T <= 262144 at N' = 64); larger configurations return MOE_ERR_UNSUPPORTED without launching.
- * The first call on a device looks up the array's device address with that device current; make
- * that first call before any stream capture. All calls share the array: calls whose kernels can
+ * The first call on a device looks up the array's device address with that device current and
+ * keeps it for the life of the process; make that first call before any stream capture, and do not
+ * reset the device (cudaDeviceReset) between calls, since the address would then be stale. All
+ * calls share the array: calls whose kernels can
  * overlap on a GPU (different streams, or several host threads) race and must be serialised by
  * the caller. No device memory is allocated or freed by this call. */
 int moe_permute_static(const moe_config* cfg, const int32_t* topk_idx, const int32_t* counts,

@@ -14,6 +14,9 @@ from oracle import OracleCfg
 NEAR_TIE = 1e-6
 # rel-L2 tolerances of h: fp32 layers / bf16 layers.
 TOL = {"f32": 1e-4, "bf16": 2e-2}
+# The same bound per token (on h and on h - u of every compared token), so that an error confined
+# to a few tokens or one expert cannot hide inside the aggregate.
+TOL_TOKEN = {"f32": 1e-3, "bf16": 5e-2}
 
 
 def rel_l2(a, b) -> float:
@@ -64,3 +67,11 @@ def check_permutation(cfg: OracleCfg, idx_gpu, offsets, perm_token, perm_slot):
     assert np.array_equal(ref["offsets"], offsets)
     assert np.array_equal(ref["perm_token"], perm_token)
     assert np.array_equal(ref["perm_slot"], perm_slot)
+
+
+def per_token_rel_l2(got, want) -> np.ndarray:
+    """rel-L2 of each row of got against the same row of want."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    den = np.linalg.norm(want, axis=1)
+    return np.linalg.norm(got - want, axis=1) / np.where(den > 0, den, 1.0)

@@ -15,7 +15,7 @@ EXPECTED = {"moe_workspace_bytes", "moe_packed_weight_bytes", "moe_pack_weights"
             "moe_permute", "moe_expert_ffn", "moe_combine", "moe_balance_stats",
             "moe_layer_forward", "moe_device_status", "moe_status_string", "moe_launch_count",
             "moe_profile_enable", "moe_profile_read", "moe_profile_read_gate_up",
-            "moe_selftest_bounded_wait"}
+            "moe_selftest_bounded_wait", "moe_layer_routing"}
 
 
 @pytest.fixture(scope="module")

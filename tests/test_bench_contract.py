@@ -78,3 +78,24 @@ def test_roofline_inputs_of_the_routed_gate_up_launch():
     assert bench.gate_up_bytes(sh, T, every_expert, with_shared=False) == want
     assert bench.gate_up_traffic("16b_bf16", "gemm_gate_up_routed") == 1141014016 + 259321856
     assert bench.gate_up_traffic("2b_bf16", "gemm_gate_up_routed") is None
+
+
+def test_layer_roofline_of_the_scope_table():
+    """The layer roofline of the 16B-like prefill is its FLOPs at the bf16 peak (2.27 TFLOP), and
+    that of the T = 64 decode its weight bytes at the HBM bandwidth (66 experts x 3 x 1408 x 2048
+    bf16 = 1.142 GB when every routed expert receives a token)."""
+    import bench
+    sh = bench.moe_inputs.CONFIGS["16b_bf16"]
+    r = bench.layer_roofline(sh, sh.T, [1] * sh.n_routed, 6500.0, 1800.0)
+    assert r["bound"] == "tensor"
+    assert abs(r["flops"] - 138.7e6 * sh.T) / r["flops"] < 1e-3
+    assert abs(r["roofline_ms"] - r["flops"] / 1.8e15 * 1e3) < 1e-9
+    dec = bench.moe_inputs.CONFIGS["16b_decode_bf16"]
+    r = bench.layer_roofline(dec, dec.T, [1] * dec.n_routed, 6500.0, 1800.0)
+    assert r["bound"] == "hbm"
+    weights = 66 * 3 * 1408 * 2048 * 2
+    assert weights < r["bytes"] < weights + 2e6
+    assert abs(r["roofline_ms"] - 0.1757) < 0.001
+    # untouched experts do not count
+    r2 = bench.layer_roofline(dec, dec.T, [1] * 32 + [0] * 32, 6500.0, 1800.0)
+    assert r2["bytes"] < r["bytes"] - 32 * 3 * 1408 * 2048 * 2 + 1

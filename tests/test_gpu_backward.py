@@ -24,25 +24,38 @@ def _shape(**kw):
     return moe_inputs.MoEShape(**base)
 
 
-def _run(shape, dh_scale=1.0, bias=None):
+def _run(shape, dh_scale=1.0, bias=None, tie=None):
+    """GPU and oracle gradients of the same objective. A near-tie token (R9: its selection is
+    decided by rounding, so the two sides may pick different experts) gets dh_t = 0: every term
+    that depends on its selection is multiplied by dh_t, and the rest of its gradient (through
+    the balance losses) depends only on the counts, which the oracle takes from the GPU. Those
+    tokens stay in the batch and in the comparison."""
     from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer
     inputs = moe_inputs.make_inputs(shape)
     if bias is not None:
         inputs["bias"] = bias
+    if tie is not None:   # expert tie[1] gets expert tie[0]'s centroid: exact ties
+        inputs["centroids"][tie[1]] = inputs["centroids"][tie[0]]
     cfg = OracleCfg.from_shape(shape)
     r = oracle.route(cfg, inputs["u"], inputs["centroids"], inputs["bias"])
-    if (r["margin"] < NEAR_TIE).any():
-        pytest.skip("seeded input has a near-tie token")   # routing would be ambiguous
+    near = r["margin"] < NEAR_TIE
     g = torch.Generator().manual_seed(shape.seed + 5)
     dh = (torch.randn(shape.T, shape.d, generator=g) * dh_scale).to(torch.bfloat16)
+    dh[torch.from_numpy(near)] = 0
     layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
                      inputs["w_up"], inputs["w_down"], inputs["bias"], backward=True)
     u = inputs["u"].to("cuda")
+    # the GPU's selection counts (the backward recomputes the same router)
+    layer.forward(u)
+    torch.cuda.synchronize()
+    counts = to_np(layer.counts).astype(np.int64)
+    idx = to_np(layer.topk_idx)
+    assert np.array_equal(idx[~near], r["topk_idx"][~near])
     got = layer.backward(u, dh.to("cuda"))
     torch.cuda.synchronize()
     from fine_grained_moe_softmax_b300 import moe_device_status
     assert moe_device_status(layer.ws_bwd) == 0
-    want = oracle.backward(cfg, inputs, dh.to(torch.float64).numpy(), r["counts"])
+    want = oracle.backward(cfg, inputs, dh.to(torch.float64).numpy(), counts)
     return {k: to_np(v) for k, v in got.items()}, want
 
 
@@ -87,100 +100,15 @@ def test_backward_2b_shape():
     _compare(got, want)
 
 
-def test_backward_zero_tokens():
-    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer
-    shape = _shape(T=16)
+def test_backward_with_near_tie_tokens():
+    """Experts 3 and 7 share a centroid, so every token that ranks them among its top K'+1 has an
+    exact tie: the near-tie rule zeroes those tokens' dh, they stay in the batch, and the
+    gradients still match the oracle's."""
+    shape = _shape(T=200, top_k=2, seed=27)
     inputs = moe_inputs.make_inputs(shape)
-    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
-                     inputs["w_up"], inputs["w_down"], backward=True)
-    g = layer.backward(torch.empty(0, shape.d, dtype=torch.bfloat16, device="cuda"),
-                       torch.empty(0, shape.d, dtype=torch.bfloat16, device="cuda"))
-    torch.cuda.synchronize()
-    for k in ("d_centroids", "d_bias", "dw_gate", "dw_up", "dw_down"):
-        assert torch.count_nonzero(g[k]) == 0
-
-
-def test_backward_full_size_sampled_du():
-    """The benchmark's 16B-like shape at its full T = 16384, in the launch configuration
-    `bench.py --backward` times: du on a seeded sample of tokens against the oracle.
-
-    du_t depends on the rest of the batch only through the selection counts, which the gradient
-    holds fixed, and through 1/T: the balance-loss part of the affinity gradient is
-    (a1 f_j + a2 f'_g) / T with f proportional to count / T. So the oracle runs on the sample with
-    the full batch's counts twice, with dh and with dh = 0. Its balance part, computed with the
-    sample's T_s, is then rescaled by (T_s / T)^2."""
-    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer, moe_device_status
-    shape = moe_inputs.CONFIGS["16b_bf16"]
-    inputs = moe_inputs.make_inputs(shape)
-    T = shape.T
-    g = torch.Generator().manual_seed(shape.seed + 5)
-    dh = torch.randn(T, shape.d, generator=g).to(torch.bfloat16)
-    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
-                     inputs["w_up"], inputs["w_down"], inputs["bias"], backward=True)
-    got = layer.backward(inputs["u"].to("cuda"), dh.to("cuda"))
-    torch.cuda.synchronize()
-    assert moe_device_status(layer.ws_bwd) == 0
-    du_gpu = to_np(got["du"])
-    del got, layer
-    torch.cuda.empty_cache()
-
-    cfg = OracleCfg.from_shape(shape)
-    r = oracle.route(cfg, inputs["u"], inputs["centroids"], inputs["bias"])
-    ok = np.nonzero(r["margin"] >= NEAR_TIE)[0]
-    rng = np.random.default_rng(11)
-    sample = np.unique(np.concatenate([ok[:2], ok[-2:], rng.choice(ok, 20, replace=False)]))
-    Ts = len(sample)
-    sub = dict(inputs)
-    sub["u"] = inputs["u"][torch.as_tensor(sample)]
-    cfg_s = OracleCfg.from_shape(shape, T=Ts)
-    dh_s = dh[torch.as_tensor(sample)].to(torch.float64).numpy()
-    w1 = oracle.backward(cfg_s, sub, dh_s, r["counts"])
-    w0 = oracle.backward(cfg_s, sub, np.zeros_like(dh_s), r["counts"])
-    du_want = w1["du"] - (1.0 - (Ts / T) ** 2) * w0["du"]
-    err = rel_l2(du_gpu[sample], du_want)
-    assert err <= TOL, f"rel-L2(du) on {Ts} sampled tokens = {err}"
-
-
-@pytest.mark.parametrize("shape", [
-    _shape(),
-    _shape(n_shared=3, inter=48, T=129, renormalize=1),
-    _shape(drop_shared=1, skip_top=1),
-    moe_inputs.CONFIGS["2b_bf16"].with_(T=300),
-], ids=["base", "3shared_renorm", "ablations", "2b"])
-def test_training_pair_matches_forward_and_backward(shape):
-    """moe_layer_forward_train + moe_layer_backward_saved run the same kernels on the same rows
-    as moe_layer_forward and moe_layer_backward, so h, the routing outputs, the statistics and
-    every gradient agree bit for bit; the saved path only skips the recompute."""
-    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer, moe_device_status
-    inputs = moe_inputs.make_inputs(shape)
-    g = torch.Generator().manual_seed(shape.seed + 5)
-    dh = torch.randn(shape.T, shape.d, generator=g).to(torch.bfloat16).to("cuda")
-    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
-                     inputs["w_up"], inputs["w_down"], inputs["bias"], backward=True)
-    u = inputs["u"].to("cuda")
-    h_ref = layer.forward(u).clone()
-    ref = {k: getattr(layer, k).clone() for k in ("topk_idx", "topk_gate", "counts", "f", "P",
-                                                   "losses")}
-    g_ref = layer.backward(u, dh)
-    torch.cuda.synchronize()
-    h = layer.forward_train(u).clone()
-    got = {k: getattr(layer, k).clone() for k in ref}
-    g_saved = layer.backward_saved(u, dh)
-    torch.cuda.synchronize()
-    assert moe_device_status(layer.ws_bwd) == 0
-    assert torch.equal(h, h_ref)
-    for k in ref:
-        assert torch.equal(got[k], ref[k]), k
-    for k in g_ref:
-        assert torch.equal(g_saved[k], g_ref[k]), k
-
-
-def test_backward_saved_needs_a_training_forward():
-    from fine_grained_moe_softmax_b300 import MoEConfig, MoELayer
-    shape = _shape(T=32)
-    inputs = moe_inputs.make_inputs(shape)
-    layer = MoELayer(MoEConfig.from_shape(shape), inputs["centroids"], inputs["w_gate"],
-                     inputs["w_up"], inputs["w_down"], backward=True)
-    u = inputs["u"].to("cuda")
-    with pytest.raises(RuntimeError):
-        layer.backward_saved(u, torch.zeros_like(u))
+    inputs["centroids"][7] = inputs["centroids"][3]
+    r = oracle.route(OracleCfg.from_shape(shape), inputs["u"], inputs["centroids"])
+    n_near = int((r["margin"] < NEAR_TIE).sum())
+    assert 5 <= n_near <= shape.T // 2
+    got, want = _run(shape, tie=(3, 7))
+    _compare(got, want)

@@ -10,7 +10,8 @@ import torch
 import moe_inputs
 import oracle
 from oracle import OracleCfg
-from parity import NEAR_TIE, TOL, check_routing, rel_l2, run_layer, to_np
+from parity import (NEAR_TIE, TOL, TOL_TOKEN, check_permutation, check_routing,
+                    per_token_rel_l2, rel_l2, run_layer, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,6 +26,12 @@ def _compare_layer(shape, inputs, layer, u_dev, tokens=None):
     gate = to_np(layer.topk_gate[:T])
     counts = to_np(layer.counts)
     ok = check_routing(cfg, ref_route, idx, gate, counts)
+    # the layer's own dispatch permutation: bit for bit the oracle's counting sort of the GPU's
+    # indices; its affinity sums against the oracle's
+    tabs = layer.routing(T)
+    check_permutation(cfg, idx, to_np(tabs["offsets"]), to_np(tabs["perm_token"]),
+                      to_np(tabs["perm_slot"]))
+    np.testing.assert_allclose(to_np(tabs["psum"]), ref_route["psum"], rtol=2e-4, atol=1e-5)
     # statistics: the oracle's balance statistics of the GPU's own counts and the oracle's psum
     st = oracle.balance_stats(cfg, counts, ref_route["psum"])
     np.testing.assert_allclose(to_np(layer.f), st["f"], rtol=1e-6)
@@ -41,6 +48,12 @@ def _compare_layer(shape, inputs, layer, u_dev, tokens=None):
     err_moe = rel_l2(h - u, fw["h"] - u)
     assert err_h <= tol, f"rel-L2(h) = {err_h}"
     assert err_moe <= tol, f"rel-L2(h - u) = {err_moe}"
+    tok_h = per_token_rel_l2(h, fw["h"])
+    tok_moe = per_token_rel_l2(h - u, fw["h"] - u)
+    worst = int(np.argmax(tok_moe))
+    assert tok_h.max() <= TOL_TOKEN[shape.dtype], f"per-token rel-L2(h) = {tok_h.max()}"
+    assert tok_moe.max() <= TOL_TOKEN[shape.dtype], \
+        f"per-token rel-L2(h - u) = {tok_moe.max()} at token {toks[worst]}"
     assert layer.device_status() == 0
     return err_h, err_moe
 
@@ -159,25 +172,39 @@ def test_near_tie_threshold_is_rare():
     assert (r["margin"] < NEAR_TIE).sum() <= 8
 
 
-def test_graph_replay_matches_direct_calls():
+@pytest.mark.parametrize("name,T", [("2b_bf16", 300), ("16b_decode_bf16", 64),
+                                    ("145b_zipf_bf16", 1000)])
+def test_graph_replay_matches_direct_calls(name, T):
     """The layer call captures into a CUDA graph; replays on new contents of the captured input
-    buffer give the same bytes as direct calls."""
-    shape = C["2b_bf16"]
-    inputs = moe_inputs.make_inputs(shape, T=300)
-    layer, u = run_layer(shape, inputs, T=300)
+    buffer give the same bytes as direct calls: the multi-tile path with the side-stream gather,
+    the one-tile decode path whose router builds the routing tables, and the 145B-like layer."""
+    shape = C[name]
+    inputs = moe_inputs.make_inputs(shape, T=T)
+    layer, u = run_layer(shape, inputs, T=T)
     graph, kernels = layer.capture(u)
     assert kernels >= 5
-    u2 = moe_inputs.make_tokens(shape, T=300, seed=99).to("cuda")
+    u2 = moe_inputs.make_tokens(shape, T=T, seed=99).to("cuda")
     u.copy_(u2)
     graph.replay()
     torch.cuda.synchronize()
     h_graph, idx_graph, P_graph = layer.h.clone(), layer.topk_idx.clone(), layer.P.clone()
+    gate_graph, loss_graph = layer.topk_gate.clone(), layer.losses.clone()
+    tabs_graph = {k: v.clone() for k, v in layer.routing(T).items()}
+    assert layer.device_status() == 0
     layer.forward(u2)
     torch.cuda.synchronize()
     assert torch.equal(h_graph, layer.h)
     assert torch.equal(idx_graph, layer.topk_idx)
+    assert torch.equal(gate_graph, layer.topk_gate)
     assert torch.equal(P_graph, layer.P)
+    assert torch.equal(loss_graph, layer.losses)
+    for k, v in layer.routing(T).items():
+        assert torch.equal(tabs_graph[k], v), k
     assert layer.device_status() == 0
+    # and the replayed routing is the oracle's
+    cfg = OracleCfg.from_shape(shape, T=T)
+    ref = oracle.route(cfg, u2.cpu(), inputs["centroids"], inputs.get("bias"))
+    check_routing(cfg, ref, to_np(idx_graph[:T]), to_np(gate_graph[:T]), to_np(layer.counts))
 
 
 def test_layer_four_times_benchmark_tokens():
@@ -190,3 +217,27 @@ def test_layer_four_times_benchmark_tokens():
     rng = np.random.default_rng(11)
     sample = np.unique(np.concatenate([[0, T - 129, T - 1], rng.choice(T, 30, replace=False)]))
     _compare_layer(shape, inputs, layer, u, tokens=sample)
+
+
+def test_routing_does_not_depend_on_the_batch_it_sits_in():
+    """A batch of one router tile splits the logits' K loop over a cluster of CTAs and adds the
+    partial sums in rank order; a large batch computes each tile in one CTA. The logits can then
+    differ in the last bits, but the routing of every token without a near-tie must be the same in
+    both, and the gates agree to the router's tolerance."""
+    shape = C["16b_bf16"]
+    big = moe_inputs.make_tokens(shape, T=16384, seed=5)
+    small = big[:64].clone()
+    inputs = moe_inputs.make_inputs(shape, T=64)
+    outs = {}
+    for name, u in (("small", small), ("big", big)):
+        inp = dict(inputs)
+        inp["u"] = u
+        layer, _ = run_layer(shape, inp, T=u.shape[0])
+        outs[name] = (to_np(layer.topk_idx[:64]), to_np(layer.topk_gate[:64]))
+        assert layer.device_status() == 0
+        del layer
+    cfg = OracleCfg.from_shape(shape, T=64)
+    ref = oracle.route(cfg, small, inputs["centroids"])
+    ok = ref["margin"] >= NEAR_TIE
+    assert np.array_equal(outs["small"][0][ok], outs["big"][0][ok])
+    assert np.abs(outs["small"][1][ok] - outs["big"][1][ok]).max() <= 2e-5

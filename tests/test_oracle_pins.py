@@ -410,3 +410,73 @@ def test_drop_shared_equals_zeroed_shared_experts(oracle_lib):
     zeroed["w_down"][:Ks] = 0
     cfg0 = OracleCfg(T=T, d=d, n_shared=Ks, n_routed=N, inter=I, top_k=2)
     np.testing.assert_array_equal(h_drop, oracle.forward_tokens(cfg0, zeroed, range(T))["h"])
+
+
+# ----------------------------------------------------------------- bf16 input path pins ----
+# bf16 inputs reach the oracle as raw 16-bit patterns, widened to double inside it. These pins
+# fix that widening against hand-written IEEE bf16 encodings and against fp32 inputs that hold
+# the same values.
+
+_BF16 = {1.0: 0x3F80, 1.5: 0x3FC0, -3.0: 0xC040, 0.5: 0x3F00, -0.5: 0xBF00, 2.0: 0x4000,
+         0.0: 0x0000}
+
+
+def test_bf16_bit_patterns_widen_to_their_values(oracle_lib):
+    """u = (1.5, -3.0) and centroids e0 = (1, 0), e1 = (0, 1), e2 = (0.5, 0.5), all given as bf16
+    bit patterns, make the logits (1.5, -3.0, -0.75): the log-ratios of the affinities are the
+    logit differences 4.5 and 2.25, so a wrong half-word, shift or sign of the widening fails."""
+    b = _BF16
+    u = np.array([[b[1.5], b[-3.0]]], np.uint16)
+    e = np.array([[b[1.0], b[0.0]], [b[0.0], b[1.0]], [b[0.5], b[0.5]]], np.uint16)
+    cfg = OracleCfg(T=1, d=2, n_shared=0, n_routed=3, inter=16, top_k=2, dtype="bf16")
+    r = oracle.route(cfg, u, e, want_scores=True)
+    s = r["scores"][0]
+    assert math.log(s[0] / s[1]) == pytest.approx(4.5, abs=1e-12)
+    assert math.log(s[0] / s[2]) == pytest.approx(2.25, abs=1e-12)
+    assert list(r["topk_idx"][0]) == [0, 2]
+
+
+def test_bf16_expert_weights_widen_to_their_values(oracle_lib):
+    """The one-hot layer of ffn_one_hot.json with every weight and token given as bf16 patterns of
+    the same (bf16-exact) values gives the same h, bit for bit, as with fp32 inputs."""
+    import torch
+    g = _golden("ffn_one_hot.json")
+    d, I, Ks, N = g["d"], g["inter"], g["n_shared"], g["n_routed"]
+    inp = _zeros_inputs(1, d, Ks, N, I)
+    for key, name in (("w_gate_nonzero", "w_gate"), ("w_up_nonzero", "w_up"),
+                      ("w_down_nonzero", "w_down")):
+        for e, a, bb, v in g[key]:
+            inp[name][e, a, bb] = v
+    inp["u"][0] = [0.0, 1.0, 1.5]
+    inp["centroids"][:] = np.float32(0.5)
+    exact = {k: torch.from_numpy(v).to(torch.bfloat16) for k, v in inp.items() if v is not None}
+    for k, v in exact.items():   # every value is exact in bf16, so the fp32 twin holds the same
+        assert np.array_equal(v.to(torch.float32).numpy(), inp[k])
+    exact["bias"] = None
+    f32 = {k: (None if v is None else v.to(torch.float32)) for k, v in exact.items()}
+    cfg16 = OracleCfg(T=1, d=d, n_shared=Ks, n_routed=N, inter=I, top_k=g["top_k"], dtype="bf16")
+    cfg32 = OracleCfg(T=1, d=d, n_shared=Ks, n_routed=N, inter=I, top_k=g["top_k"])
+    h16 = oracle.forward_tokens(cfg16, exact, [0])["h"]
+    h32 = oracle.forward_tokens(cfg32, f32, [0])["h"]
+    np.testing.assert_array_equal(h16, h32)
+    assert np.any(h16 != inp["u"])   # the experts contribute
+
+
+def test_bf16_inputs_equal_fp32_inputs_of_the_same_values(oracle_lib):
+    """Seeded bf16 tensors of the 2B-like layer (sub-sampled) against fp32 tensors holding the
+    same values: routing, margins, sums and h agree exactly."""
+    import torch
+    sh = moe_inputs.CONFIGS["2b_bf16"].with_(T=12, d=64, n_routed=16, inter=32, top_k=4,
+                                            n_groups=4)
+    inp = moe_inputs.make_inputs(sh)
+    f32 = {k: (None if v is None else v.to(torch.float32)) for k, v in inp.items()}
+    f32["bias"] = inp["bias"]
+    c16 = OracleCfg.from_shape(sh)
+    c32 = OracleCfg.from_shape(sh.with_(dtype="f32"))
+    r16 = oracle.route(c16, inp["u"], inp["centroids"], want_scores=True)
+    r32 = oracle.route(c32, f32["u"], f32["centroids"], want_scores=True)
+    for k in ("scores", "topk_idx", "topk_gate", "margin", "counts", "psum"):
+        np.testing.assert_array_equal(r16[k], r32[k])
+    toks = np.arange(sh.T)
+    np.testing.assert_array_equal(oracle.forward_tokens(c16, inp, toks)["h"],
+                                  oracle.forward_tokens(c32, f32, toks)["h"])

@@ -92,3 +92,36 @@ def test_static_reports_corrupt_counts_and_rejects_oversized():
     big = B.MoEConfig.from_shape(shape, T=128 * 2100)   # 2100 tiles x 63 experts > the limit
     assert fn(ctypes.byref(big), _p(idx), _p(counts), _p(idx), _p(idx), _p(idx), None,
               None) == -2
+
+
+def test_static_at_its_size_limit():
+    """ceil(T / 128) * N' exactly at the documented limit of 131072 table entries (8192 tiles of
+    128 tokens, N' = 16) reaches the far end of both tables in the fixed array; the result must
+    equal moe_permute's and the oracle's counting sort. One token more must be refused."""
+    import oracle
+    from oracle import OracleCfg
+    B, fn = _lib()
+    shape = moe_inputs.MoEShape("limit", T=128 * 8192, d=64, n_shared=0, n_routed=16, inter=16,
+                                top_k=2, n_groups=1, dtype="bf16", seed=0)
+    T, K, N = shape.T, shape.top_k, shape.n_routed
+    g = torch.Generator().manual_seed(77)
+    first = torch.randint(0, N, (T,), generator=g)
+    second = (first + torch.randint(1, N, (T,), generator=g)) % N
+    idx = torch.stack([first, second], 1).to(torch.int32)
+    counts = torch.bincount(idx.flatten().long(), minlength=N).to(torch.int32)
+    cfg = B.MoEConfig.from_shape(shape)
+    dev = "cuda"
+    ws = torch.empty(B.moe_workspace_bytes(cfg), dtype=torch.uint8, device=dev)
+    out = _run_both(B, fn, cfg, ws, idx.to(dev), counts.to(dev))
+    for a, b in zip(out["ref"][:3], out["static"][:3]):
+        assert torch.equal(a, b)
+    assert out["ws_status"] == 0 and int(out["static"][3][0]) == 0
+    want = oracle.permute(OracleCfg.from_shape(shape), idx.numpy())
+    off, pt, ps = (t.numpy() for t in out["static"][:3])
+    assert np.array_equal(off, want["offsets"])
+    assert np.array_equal(pt, want["perm_token"])
+    assert np.array_equal(ps, want["perm_slot"])
+    over = B.MoEConfig.from_shape(shape, T=T + 1)   # 8193 tiles x 16 experts
+    d_idx = idx.to(dev)
+    assert fn(ctypes.byref(over), _p(d_idx), _p(d_idx), _p(d_idx), _p(d_idx), _p(d_idx), None,
+              None) == -2
