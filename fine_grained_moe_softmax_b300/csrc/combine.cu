@@ -117,36 +117,13 @@ __global__ void balance_kernel(Dims m, const int* __restrict__ counts,
                                float* __restrict__ P_out, float* __restrict__ losses) {
     __shared__ float f_s[kMaxRouted], P_s[kMaxRouted];
     const int N = m.N;
-    const float Tf = (float)max(m.T, 1);
-    const float scale = (float)N / ((float)m.K * Tf);
     for (int j = threadIdx.x; j < N; j += blockDim.x) {
-        const float f = scale * (float)counts[j];
-        const float P = psum[j] / Tf;
-        f_s[j] = f;
-        P_s[j] = P;
-        f_out[j] = f;
-        P_out[j] = P;
+        balance_fp(m, counts[j], psum[j], &f_s[j], &P_s[j]);
+        f_out[j] = f_s[j];
+        P_out[j] = P_s[j];
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        float lexp = 0.f;
-        for (int j = 0; j < N; ++j) lexp += f_s[j] * P_s[j];
-        float ldev = 0.f;
-        const int base = N / m.D, extra = N % m.D;
-        int first = 0;
-        for (int g = 0; g < m.D; ++g) {
-            const int size = base + (g < extra ? 1 : 0);
-            float fs = 0.f, ps = 0.f;
-            for (int j = first; j < first + size; ++j) {
-                fs += f_s[j];
-                ps += P_s[j];
-            }
-            ldev += (fs / (float)size) * ps;
-            first += size;
-        }
-        losses[0] = m.a1 * lexp;
-        losses[1] = m.a2 * ldev;
-    }
+    if (threadIdx.x < 32) balance_losses_warp(m, f_s, P_s, losses, threadIdx.x);
 }
 
 }  // namespace

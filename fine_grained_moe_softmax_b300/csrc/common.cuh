@@ -176,8 +176,8 @@ inline BwdLayout bwd_layout(const Dims& m) {
 // Balance statistics in one fixed order shared by every kernel that produces them:
 //   f_j = N' / (K' T) count_j and P_j = psum_j / T (balance_fp, one expert at a time), then
 //   L_ExpBal = a1 sum_j f_j P_j and L_DevBal = a2 sum_g mean_{j in G_g}(f_j) * sum_{j in G_g} P_j
-//   over D contiguous groups, the first N' mod D one expert larger (balance_losses, one thread,
-//   from the f_j and P_j already computed).
+//   over D contiguous groups, the first N' mod D one expert larger (balance_losses_warp, one whole
+//   warp, from the f_j and P_j already computed).
 __device__ inline void balance_fp(const Dims& m, int total_j, float ptot_j, float* f_j,
                                   float* P_j) {
     const float Tf = (float)max(m.T, 1);
@@ -186,25 +186,34 @@ __device__ inline void balance_fp(const Dims& m, int total_j, float ptot_j, floa
     *P_j = ptot_j / Tf;
 }
 
-__device__ inline void balance_losses(const Dims& m, const float* f, const float* P,
-                                      float* losses) {
+// Called by all 32 lanes of one warp (f, P in shared memory). Lane l sums experts l, l + 32, ...
+// and groups l, l + 32, ... in ascending order; a fixed butterfly adds the lanes, so every kernel
+// that calls it gets the same bits. Lane 0 writes losses[0..1].
+__device__ inline void balance_losses_warp(const Dims& m, const float* f, const float* P,
+                                           float* losses, int lane) {
     const int N = m.N;
     float lexp = 0.f, ldev = 0.f;
-    for (int j = 0; j < N; ++j) lexp += f[j] * P[j];
+    for (int j = lane; j < N; j += 32) lexp = __fmaf_rn(f[j], P[j], lexp);
     const int base = N / m.D, extra = N % m.D;
-    int first = 0;
-    for (int g = 0; g < m.D; ++g) {
+    for (int g = lane; g < m.D; g += 32) {
         const int size = base + (g < extra ? 1 : 0);
+        const int first = g * base + (g < extra ? g : extra);
         float fs = 0.f, ps = 0.f;
         for (int j = first; j < first + size; ++j) {
             fs += f[j];
             ps += P[j];
         }
-        ldev += (fs / (float)size) * ps;
-        first += size;
+        ldev = __fmaf_rn(fs / (float)size, ps, ldev);
     }
-    losses[0] = m.a1 * lexp;
-    losses[1] = m.a2 * ldev;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lexp += __shfl_xor_sync(0xffffffffu, lexp, o);
+        ldev += __shfl_xor_sync(0xffffffffu, ldev, o);
+    }
+    if (lane == 0) {
+        losses[0] = m.a1 * lexp;
+        losses[1] = m.a2 * ldev;
+    }
 }
 
 // First error wins; later errors leave the word alone.

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(1024) route_finalize_kernel(FinalizeArgs a) {
         for (int j = threadIdx.x; j < N; j += blockDim.x)
             balance_fp(m, total[j], ptot[j], &fs[j], &Ps[j]);
     __syncthreads();
-    if (threadIdx.x == 32 && a.losses) balance_losses(m, fs, Ps, a.losses);
+    if (warp == 1 && a.losses) balance_losses_warp(m, fs, Ps, a.losses, lane);
     __syncthreads();
     if (a.offsets)
         for (int j = threadIdx.x; j <= N; j += blockDim.x) a.offsets[j] = off[j];

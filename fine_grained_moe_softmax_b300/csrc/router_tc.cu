@@ -10,11 +10,17 @@
 // accumulating fp32 logits in TMEM. When there are few tiles (decode-sized batches), a cluster of
 // C CTAs shares a tile, each over 1/C of d; the other CTAs leave their partial logits in their
 // shared memory and the first adds them to its own, in rank order, through distributed shared
-// memory, so the sum does not depend on timing. Four epilogue warps then own one token per thread: each reads
-// its logit row from TMEM once (warp w sees TMEM lanes 32*(w%4) .. +31), adds the optional bias,
-// keeps the row in the (by then idle) TMA ring, and computes the softmax, a register top-K'
-// (ranked by logit; the lower index wins ties), the gates, the tile's expert histogram and, by a
-// warp transpose-reduction, the tile's per-expert sums of affinities in a fixed order.
+// memory, so the sum does not depend on timing.
+//
+// Sixteen epilogue warps route the tile: four per TMEM lane quarter (warp w reads lanes
+// 32*(w%4) .. +31), each over a quarter of the expert columns. A thread owns one token of one
+// column slice: it reads the slice's logits from TMEM once, adds the optional bias, keeps them in
+// the (by then idle) TMA ring, and keeps the slice's maximum and its top list (ranked by logit, the
+// lower index first on ties). The slices' maxima give the softmax shift, their exponential sums
+// (added in slice order) the denominator, and a shuffle transpose the tile's per-expert sums of
+// affinities in a fixed order. The four slice lists of a token are merged by four lanes, one list
+// each, in K' rounds of a 4-way maximum whose ties go to the lower slice (the lower indices);
+// those lanes then write the token's experts and gates and count the tile's histogram.
 #include <math.h>
 
 #include "common.cuh"
@@ -28,12 +34,19 @@ namespace {
 
 constexpr int RBM = 128;
 constexpr int RBK = 64;
-constexpr int kThreads = 192;
+constexpr int kEpiWarpsBwd = 4;                        // backward: one warp per lane quarter
+constexpr int kEpiWarpsFwd = 16;                       // forward: four per lane quarter
 constexpr int kMaxStages = 8;
 
-struct RouterArgs {
-    CUtensorMap a;        // u [T, d], box [128 x 64]
-    CUtensorMap b;        // centroids [N', d], box [n_pad x 64]
+__host__ __device__ constexpr int router_threads(bool bwd) {
+    return 64 + 32 * (bwd ? kEpiWarpsBwd : kEpiWarpsFwd);
+}
+
+// Scalar arguments of the router kernel. Kernel code reads them from a copy in shared memory (or
+// from registers): the kernel takes the tensor maps' addresses, which makes every direct read of
+// a kernel argument a generic load of the argument buffer, and the mbarrier waits' memory
+// clobbers would otherwise force such a reload on every pipeline step.
+struct RouterParams {
     const float* bias;    // [N'] or null
     int T, N, K, renorm, skip, k_blocks, n_pad, stages, tmem_cols;
     int csize;            // CTAs per tile (cluster size); CTA r takes K blocks [r kb/C, (r+1) kb/C)
@@ -61,6 +74,13 @@ struct RouterArgs {
     int* perm_slot;       // [T K']
     float *f_out, *P_out, *losses;   // balance statistics, or null
 };
+
+struct RouterArgs {
+    CUtensorMap a;        // u [T, d], box [128 x 64]
+    CUtensorMap b;        // centroids [N', d], box [n_pad x 64]
+    RouterParams p;
+};
+static_assert(sizeof(RouterParams) % 8 == 0, "copied in 4-byte words");
 
 template <int KMAX>
 struct TopK {
@@ -117,27 +137,68 @@ __device__ __forceinline__ float column_sums(float (&v)[32], int lane) {
     return v[0];
 }
 
-__device__ __forceinline__ void epilogue_bar() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+// One halving step with the shuffle partner at lane distance MASK: lanes with `upper` clear keep
+// columns [0, HALF) and receive the partner's, lanes with it set keep [HALF, 2*HALF).
+template <int HALF, int MASK>
+__device__ __forceinline__ void halve_x(float (&v)[8], bool upper) {
+#pragma unroll
+    for (int i = 0; i < HALF; ++i) {
+        const float send = upper ? v[i] : v[i + HALF];
+        const float keep = upper ? v[i + HALF] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
+    }
 }
 
-// The routing tables of a one-tile batch, by the four epilogue warps (et = 0..127, thread et = token
-// et) after the tile is routed: totals, offsets (exclusive scan, segments padded to a.pad), the
-// balance statistics and the stable permutation. The rank of token t in expert j is the number of
-// earlier tokens of the tile choosing j (a prefix popcount of j's token bitmap); these are the
-// results of the finalize and scatter kernels for the same batch, bit for bit. `scratch` is the
-// idle TMA ring. Every epilogue warp runs the whole sequence (the barriers need all four).
-__device__ __noinline__ void finish_single_tile(const RouterArgs& a, uint8_t* scratch,
+// After this, lane l of the warp holds the sum over the 32 lanes of column (l >> 2) & 7 of
+// v[0..7] (lanes 4c .. 4c+3 hold column c), added in one fixed pattern.
+__device__ __forceinline__ float column_sums8(float (&v)[8], int lane) {
+    halve_x<4, 16>(v, lane & 16);
+    halve_x<2, 8>(v, lane & 8);
+    halve_x<1, 4>(v, lane & 4);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return v[0];
+}
+
+template <int THREADS>
+__device__ __forceinline__ void epilogue_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+}
+
+// Barrier of the epilogue warps that also returns 1 only if v != 0 in every one of their threads.
+template <int THREADS>
+__device__ __forceinline__ int epilogue_and(int v) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v), "n"(THREADS)
+        : "memory");
+    return r;
+}
+
+// The routing tables of a one-tile batch, by the sixteen epilogue warps (et = 0..511) after the
+// tile is routed: totals, offsets (exclusive scan, segments padded to a.pad), the balance
+// statistics and the stable permutation. The rank of token t in expert j is the number of earlier
+// tokens of the tile choosing j (a prefix popcount of j's token bitmap); these are the results of
+// the finalize and scatter kernels for the same batch, bit for bit. `scratch` is the idle TMA
+// ring. Every epilogue warp runs the whole sequence (the barriers need all of them).
+constexpr int kEpiThreadsFwd = 32 * kEpiWarpsFwd;
+
+__device__ __noinline__ void finish_single_tile(const RouterParams& a, uint8_t* scratch,
                                                 const int* hist, const float* colsum,
-                                                const int* chosen, int et, int lane) {
-    const int N = a.N, K = a.K, T = a.T;
+                                                const int* chosen, int et) {
+    const int N = a.N, K = a.K, T = a.T, lane = et & 31;
     uint32_t* bits = reinterpret_cast<uint32_t*>(scratch);         // [N'][4]: tokens 0..127
     int* off = reinterpret_cast<int*>(bits + 4 * kMaxRouted);       // [N' + 1]
     float* ptot = reinterpret_cast<float*>(off + kMaxRouted + 1);   // [N']
     float* fs = ptot + kMaxRouted;                                  // [N']
     float* Ps = fs + kMaxRouted;                                    // [N']
-    for (int i = et; i < 4 * N; i += 128) bits[i] = 0u;
-    for (int j = et; j < N; j += 128) {
+    for (int i = et; i < 4 * N; i += kEpiThreadsFwd) bits[i] = 0u;
+    for (int j = et; j < N; j += kEpiThreadsFwd) {
         const float col = ((colsum[j] + colsum[kMaxRouted + j]) + colsum[2 * kMaxRouted + j]) +
                           colsum[3 * kMaxRouted + j];
         ptot[j] = col;
@@ -145,141 +206,217 @@ __device__ __noinline__ void finish_single_tile(const RouterArgs& a, uint8_t* sc
         a.psum_out[j] = col;
         balance_fp(a.dims, hist[j], col, &fs[j], &Ps[j]);
     }
-    epilogue_bar();
-    const int t = et;
-    if (t < T)
-        for (int k = 0; k < K; ++k) {
-            const int j = chosen[t * kMaxTopK + k];
-            if (j >= 0 && j < N) atomicOr(&bits[j * 4 + (t >> 5)], 1u << (t & 31));
-        }
+    epilogue_bar<kEpiThreadsFwd>();
+    for (int x = et; x < T * K; x += kEpiThreadsFwd) {
+        const int t = x / K, j = chosen[t * kMaxTopK + x % K];
+        if (j >= 0 && j < N) atomicOr(&bits[j * 4 + (t >> 5)], 1u << (t & 31));
+    }
     if (et < 32) {   // offsets: lane l scans experts 8l .. 8l+7 (N' <= 256)
-        int loc[8], sum = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int j = lane * 8 + q;
-            const int v = j < N ? (a.pad > 0 ? (hist[j] + a.pad - 1) / a.pad * a.pad : hist[j]) : 0;
-            loc[q] = sum;
-            sum += v;
-        }
+        const int pad = a.pad;
+        int sum = 0;
+#pragma unroll 1
+        for (int j = lane * 8; j < min(lane * 8 + 8, N); ++j)
+            sum += pad > 0 ? (hist[j] + pad - 1) / pad * pad : hist[j];
         int incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int j = lane * 8 + q;
-            if (j < N) off[j] = incl - sum + loc[q];
+        int run = incl - sum;
+#pragma unroll 1
+        for (int j = lane * 8; j < min(lane * 8 + 8, N); ++j) {
+            off[j] = run;
+            run += pad > 0 ? (hist[j] + pad - 1) / pad * pad : hist[j];
         }
         if (lane == 31) off[N] = incl;
+    } else if (et < 64 && a.losses) {
+        balance_losses_warp(a.dims, fs, Ps, a.losses, lane);
     }
-    epilogue_bar();
-    for (int j = et; j <= N; j += 128) a.offsets[j] = off[j];
-    if (et == 32 && a.losses) balance_losses(a.dims, fs, Ps, a.losses);
+    epilogue_bar<kEpiThreadsFwd>();
+    for (int j = et; j <= N; j += kEpiThreadsFwd) a.offsets[j] = off[j];
     if (a.f_out)
-        for (int j = et; j < N; j += 128) {
+        for (int j = et; j < N; j += kEpiThreadsFwd) {
             a.f_out[j] = fs[j];
             a.P_out[j] = Ps[j];
         }
-    if (t < T)
-        for (int k = 0; k < K; ++k) {
-            int j = chosen[t * kMaxTopK + k];
-            j = (j >= 0 && j < N) ? j : 0;
-            int rank = __popc(bits[j * 4 + (t >> 5)] & ((1u << (t & 31)) - 1u));
-            for (int w = 0; w < (t >> 5); ++w) rank += __popc(bits[j * 4 + w]);
-            const int row = off[j] + rank;
-            a.perm_slot[(size_t)t * K + k] = row;
-            a.perm_token[row] = t;
-        }
+    for (int x = et; x < T * K; x += kEpiThreadsFwd) {
+        const int t = x / K;
+        int j = chosen[t * kMaxTopK + x % K];
+        j = (j >= 0 && j < N) ? j : 0;
+        int rank = __popc(bits[j * 4 + (t >> 5)] & ((1u << (t & 31)) - 1u));
+        for (int w = 0; w < (t >> 5); ++w) rank += __popc(bits[j * 4 + w]);
+        const int row = off[j] + rank;
+        a.perm_slot[x] = row;
+        a.perm_token[row] = t;
+    }
 }
 
-// Routing of the 128 tokens of a tile by the four epilogue warps (thread = token): softmax over
-// the N' routed experts, top-K' by logit (lower index on ties), gates, the tile histogram and the
-// tile's per-expert affinity sums. `zc` ([n_pad][128] floats, column j of row r at j * 128 + r,
-// conflict-free per warp) receives the biased logits and then the exponentials, so TMEM is read
-// once and every exponential is computed once.
+// Routing of the tile's tokens by the sixteen epilogue warps. Warp w (2 <= w < 18) reads TMEM lane
+// quarter q = w % 4 (tokens 32q .. 32q+31) and column slice h = (w - 2) / 4 of n_pad / 4 columns.
+// Shared scratch: zc = [n_pad][128] floats at the start of the idle ring (column j of token row r
+// at j * 128 + r, conflict-free per warp), then the slice lists [4][KMAX][128] (values, then
+// indices); `red` holds the slices' maxima and exponential sums [2][4][128].
 template <int KMAX>
-__device__ __forceinline__ void route_tile(const RouterArgs& a, uint32_t tmem_lanes, float* zc,
-                                          int tile, int quarter, int lane, float* colsum,
-                                          int* hist, const float* bias_s, int* chosen) {
+__device__ __forceinline__ void route_tile(const RouterParams& a, uint32_t tmem, uint8_t* ring,
+                                          int tile, int warp, int lane, float* colsum, int* hist,
+                                          const float* bias_s, int* chosen, float* chosen_s,
+                                          float* red) {
     const int N = a.N, K = a.K;
-    const int row = quarter * 32 + lane;
-    const int t = tile * RBM + row;
-    const bool valid = t < a.T;
-    const int n_chunks = a.n_pad / 32;
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const int rows_valid = min(RBM, a.T - tile * RBM);
+    const bool valid = row < rows_valid;
+    const int cs = a.n_pad >> 2;   // columns per slice, a multiple of 8
+    const int c0 = h * cs;
+    float* zc = reinterpret_cast<float*>(ring);
+    float* lv = zc + a.n_pad * RBM;
+    int* li = reinterpret_cast<int*>(lv + 4 * KMAX * RBM);
+    float* red_max = red;
+    float* red_sum = red + 4 * RBM;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     // the other CTAs of the cluster keep their partial logits at the same offset as zc
     const uint32_t part = ptx::smem_addr(zc);
-    // pass 1 (TMEM): biased logits, their maximum and the top list
-    float zmax = -INFINITY;
+
+    // A: the slice's biased logits, their maximum and the slice's top list. The epilogue runs once
+    // per launch, so its code is fetched cold: loops stay rolled where unrolling buys nothing.
+    float mloc = -INFINITY;
     TopK<KMAX> top;
     top.init();
-    for (int c = 0; c < n_chunks; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(tmem_lanes + c * 32, v);
+#pragma unroll 1
+    for (int c = c0; c < c0 + cs; c += 8) {
+        uint32_t v[8];
+        ptx::tmem_ld_32x32b_x8(tl + c, v);
         ptx::tmem_ld_wait();
-        for (int r = 1; r < a.csize; ++r) {   // partial sums of the later K slices, in rank order
-            const uint32_t peer = ptx::mapa(part, (uint32_t)r);
-            float pv[32];
+        if (valid && a.csize > 1) {
+            // partial sums of the later K slices, added in rank order; the loads of all the
+            // cluster's CTAs for four columns are issued before any of them is used
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                pv[i] = ptx::ld_cluster_f32(peer + (uint32_t)(((c * 32 + i) * RBM + row) * 4));
+            for (int h4 = 0; h4 < 8; h4 += 4) {
+                float pv[7][4];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + pv[i]);
-        }
+                for (int r = 1; r < 8; ++r)
+                    if (r < a.csize) {
+                        const uint32_t peer = ptx::mapa(part, (uint32_t)r);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int j = c * 32 + i;
-            if (j < N) {
-                const float z = __uint_as_float(v[i]) + bias_s[j];
-                zc[j * RBM + row] = z;
-                zmax = fmaxf(zmax, z);
-                top.push(z, j);
+                        for (int i = 0; i < 4; ++i)
+                            pv[r - 1][i] = ptx::ld_cluster_f32(
+                                peer + (uint32_t)(((c + h4 + i) * RBM + row) * 4));
+                    }
+#pragma unroll
+                for (int r = 1; r < 8; ++r)
+                    if (r < a.csize) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            v[h4 + i] = __float_as_uint(__uint_as_float(v[h4 + i]) + pv[r - 1][i]);
+                    }
             }
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) zc[(c + i) * RBM + row] = __uint_as_float(v[i]);
+        const int c_end = min(c + 8, N);
+#pragma unroll 1
+        for (int j = c; j < c_end; ++j) {
+            const float z = zc[j * RBM + row] + bias_s[j];
+            zc[j * RBM + row] = z;
+            mloc = fmaxf(mloc, z);
+            top.push(z, j);
+        }
     }
-    // pass 2: exponentials and the softmax denominator
-    float sum = 0.f;
-    for (int j = 0; j < N; ++j) {
+    red_max[h * RBM + row] = mloc;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        lv[(h * KMAX + k) * RBM + row] = top.v[k];
+        li[(h * KMAX + k) * RBM + row] = top.i[k];
+    }
+    epilogue_bar<kEpiThreadsFwd>();
+
+    // B: exponentials of the slice and its part of the softmax denominator
+    const float zmax = fmaxf(fmaxf(red_max[row], red_max[RBM + row]),
+                             fmaxf(red_max[2 * RBM + row], red_max[3 * RBM + row]));
+    float ssum = 0.f;
+    const int c1 = min(c0 + cs, N);
+    for (int j = c0; j < c1; ++j) {
         const float e = __expf(zc[j * RBM + row] - zmax);
         zc[j * RBM + row] = e;
-        sum += e;
+        ssum += e;
     }
-    const float inv = 1.0f / sum;
-    if (valid) {
+    red_sum[h * RBM + row] = ssum;
+    epilogue_bar<kEpiThreadsFwd>();
+
+    // C: the slice's affinities summed over the warp's 32 tokens, per expert column
+    {
+        const float inv = 1.0f / (((red_sum[row] + red_sum[RBM + row]) + red_sum[2 * RBM + row]) +
+                                  red_sum[3 * RBM + row]);
+        for (int c = c0; c < c0 + cs; c += 8) {
+            float sv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = c + i;
+                sv[i] = (valid && j < N) ? zc[j * RBM + row] * inv : 0.f;
+            }
+            const float col = column_sums8(sv, lane);
+            if ((lane & 3) == 0) colsum[q * kMaxRouted + c + (lane >> 2)] = col;
+        }
+    }
+
+    // D: merge of the token's four slice lists by four lanes (lane & 3 = the list it reads), one
+    // rank per round; the chosen ranks' experts and affinities go to `chosen` / `chosen_s`
+    {
+        const int tr = q * 32 + h * 8 + (lane >> 2);
+        const int sub = lane & 3;
+        const bool tvalid = tr < rows_valid;
+        const float zm = fmaxf(fmaxf(red_max[tr], red_max[RBM + tr]),
+                               fmaxf(red_max[2 * RBM + tr], red_max[3 * RBM + tr]));
+        const float tinv = 1.0f / (((red_sum[tr] + red_sum[RBM + tr]) + red_sum[2 * RBM + tr]) +
+                                   red_sum[3 * RBM + tr]);
         const int q0 = a.skip;   // chosen ranks: q0 .. q0+K'-1
+        int p = 0;
         float gsum = 0.f;
+        bool bad = !(zm < INFINITY);
+#pragma unroll 1
+        for (int r = 0; r < q0 + K; ++r) {
+            float v = p < KMAX ? lv[(sub * KMAX + p) * RBM + tr] : -INFINITY;
+            int ix = p < KMAX ? li[(sub * KMAX + p) * RBM + tr] : -1;
+            int sl = sub;
 #pragma unroll
-        for (int q = 0; q < KMAX; ++q)
-            if (q >= q0 && q < q0 + K) gsum += __expf(top.v[q] - zmax) * inv;
-        bool bad = !(zmax < INFINITY);
-#pragma unroll
-        for (int q = 0; q < KMAX; ++q) {
-            if (q >= q0 && q < q0 + K) {
-                int j = top.i[q];
-                if (j < 0) {
-                    bad = true;
-                    j = 0;
+            for (int m = 1; m <= 2; m <<= 1) {   // 4-way maximum; ties to the lower slice
+                const float ov = __shfl_xor_sync(0xffffffffu, v, m);
+                const int oi = __shfl_xor_sync(0xffffffffu, ix, m);
+                const int os = __shfl_xor_sync(0xffffffffu, sl, m);
+                if (ov > v || (ov == v && os < sl)) {
+                    v = ov;
+                    ix = oi;
+                    sl = os;
                 }
-                const float s = __expf(top.v[q] - zmax) * inv;
-                a.topk_idx[(size_t)t * K + q - q0] = j;
-                a.topk_gate[(size_t)t * K + q - q0] = a.renorm ? s / gsum : s;
-                chosen[row * kMaxTopK + q - q0] = j;   // for the one-tile tables
-                atomicAdd(&hist[j], 1);
+            }
+            if (sl == sub) ++p;
+            if (r >= q0) {
+                const float sj = __expf(v - zm) * tinv;
+                gsum += sj;
+                if (ix < 0) {
+                    bad = true;
+                    ix = 0;
+                }
+                if (sub == 0) {
+                    chosen[tr * kMaxTopK + r - q0] = ix;   // also for the one-tile tables
+                    chosen_s[tr * kMaxTopK + r - q0] = sj;
+                }
             }
         }
-        if (bad) set_status(a.status, MOE_ERR_CORRUPT_INPUT);
-    }
-    // pass 3: affinities, summed over this warp's 32 tokens per expert column
-    for (int c = 0; c < n_chunks; ++c) {
-        float s[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int j = c * 32 + i;
-            s[i] = (valid && j < N) ? zc[j * RBM + row] * inv : 0.f;
+        __syncwarp();
+        if (tvalid) {
+            const int t = tile * RBM + tr;
+#pragma unroll 1
+            for (int k = sub; k < K; k += 4) {
+                const int j = chosen[tr * kMaxTopK + k];
+                const float sj = chosen_s[tr * kMaxTopK + k];
+                a.topk_idx[(size_t)t * K + k] = j;
+                a.topk_gate[(size_t)t * K + k] = a.renorm ? sj / gsum : sj;
+                atomicAdd(&hist[j], 1);
+            }
+            if (bad && sub == 0) set_status(a.status, MOE_ERR_CORRUPT_INPUT);
         }
-        const float col = column_sums(s, lane);
-        colsum[quarter * kMaxRouted + c * 32 + lane] = col;
     }
 }
 
@@ -288,7 +425,7 @@ __device__ __forceinline__ void route_tile(const RouterArgs& a, uint32_t tmem_la
 // balance-loss term (a1 f_j + a2 f'_group(j)) / T, and dz_j = s_j (ds_j - sum_m s_m ds_m).
 // dz is written as bf16 [T, n_pad] (zero past N'); its per-tile column sums (for the bias
 // gradient) go through the same fixed-order warp reduction as the affinity sums.
-__device__ __forceinline__ void route_tile_bwd(const RouterArgs& a, uint32_t tmem_lanes, float* zc,
+__device__ __forceinline__ void route_tile_bwd(const RouterParams& a, uint32_t tmem_lanes, float* zc,
                                               int tile, int quarter, int lane, float* colsum,
                                               const float* bias_s, const float* aux_s) {
     const int N = a.N, K = a.K;
@@ -378,11 +515,16 @@ __device__ __forceinline__ void route_tile_bwd(const RouterArgs& a, uint32_t tme
 }
 
 template <int KMAX, bool BWD>
-__global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_constant__ RouterArgs a) {
+__global__ void __launch_bounds__(router_threads(BWD), 1)
+    router_tc_kernel(const __grid_constant__ RouterArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t ring = a.stages * a.stage_bytes;
+    // scalars read once into registers (the copy in shared memory serves the epilogue)
+    const int stages = a.p.stages, csize = a.p.csize, k_blocks = a.p.k_blocks, N = a.p.N;
+    const uint32_t stage_bytes = a.p.stage_bytes;
+    int* const status = a.p.status;
+    const uint32_t ring = stages * stage_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(base + ring);
     uint64_t* empty = full + kMaxStages;
     uint64_t* tfull = empty + kMaxStages;
@@ -394,18 +536,20 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     float* bias_s = reinterpret_cast<float*>(hist + kMaxRouted);  // [kMaxRouted]
     float* aux_s = bias_s + kMaxRouted;                           // [kMaxRouted] (backward)
     int* chosen = reinterpret_cast<int*>(aux_s + kMaxRouted);     // [128][kMaxTopK]
+    float* chosen_s = reinterpret_cast<float*>(chosen + RBM * kMaxTopK);   // [128][kMaxTopK]
+    float* red = chosen_s + RBM * kMaxTopK;                               // [2][4][128] (forward)
+    RouterParams* ps = reinterpret_cast<RouterParams*>(red + 2 * 4 * RBM);   // the scalars
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int crank = a.csize > 1 ? (int)ptx::cluster_ctarank() : 0;
+    const int crank = csize > 1 ? (int)ptx::cluster_ctarank() : 0;
     const bool leader = crank == 0;
-    const int tile = blockIdx.x / a.csize;
-    const int n_tiles = gridDim.x / a.csize;
-    const int kb_begin = crank * a.k_blocks / a.csize;
-    const int kb_end = (crank + 1) * a.k_blocks / a.csize;
-    const int N = a.N;
+    const int tile = blockIdx.x / csize;
+    const int n_tiles = gridDim.x / csize;
+    const int kb_begin = crank * k_blocks / csize;
+    const int kb_end = (crank + 1) * k_blocks / csize;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < a.stages; ++s) {
+        for (int s = 0; s < stages; ++s) {
             ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
         }
@@ -420,24 +564,35 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
         ptx::prefetch_tmap(&a.b);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), a.tmem_cols);
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), a.p.tmem_cols);
         ptx::tmem_relinquish();
+    }
+    if (warp == 2) {   // the epilogue's copy of the scalars (ordered by the epilogue's barriers)
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(&a.p);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(ps);
+        for (int i = lane; i < (int)(sizeof(RouterParams) / 4); i += 32) dst[i] = src[i];
     }
     pdl_wait();
     pdl_trigger();
-    for (int j = threadIdx.x; j < kMaxRouted; j += blockDim.x)
-        bias_s[j] = (a.bias && j < N) ? a.bias[j] : 0.f;
+    {
+        const float* bias = a.p.bias;
+        for (int j = threadIdx.x; j < kMaxRouted; j += blockDim.x)
+            bias_s[j] = (bias && j < N) ? bias[j] : 0.f;
+    }
     if constexpr (BWD) {   // balance-loss gradient per expert: (a1 f_j + a2 f'_group(j)) / T
-        const float Tf = (float)a.T, scale = (float)N / ((float)a.K * Tf);
-        const int gbase = N / a.D, extra = N % a.D;
+        const int* counts = a.p.counts;
+        const int K = a.p.K, D = a.p.D;
+        const float Tf = (float)a.p.T, scale = (float)N / ((float)K * Tf);
+        const float a1 = a.p.a1, a2 = a.p.a2;
+        const int gbase = N / D, extra = N % D;
         for (int j = threadIdx.x; j < N; j += blockDim.x) {
             const int g = j < extra * (gbase + 1) ? j / (gbase + 1)
                                                   : extra + (j - extra * (gbase + 1)) / gbase;
             const int first = g * gbase + (g < extra ? g : extra);
             const int size = gbase + (g < extra ? 1 : 0);
             float fs = 0.f;
-            for (int q = first; q < first + size; ++q) fs += scale * (float)a.counts[q];
-            aux_s[j] = (a.a1 * scale * (float)a.counts[j] + a.a2 * fs / (float)size) / Tf;
+            for (int q = first; q < first + size; ++q) fs += scale * (float)counts[q];
+            aux_s[j] = (a1 * scale * (float)counts[j] + a2 * fs / (float)size) / Tf;
         }
     }
     ptx::tc_fence_before();
@@ -453,25 +608,25 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
             int issued = 0;
             bool ok = true;
             for (int kb = kb_begin; kb < kb_end; ++kb) {
-                if (!wait_phase(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag, a.status)) {
+                if (!wait_phase(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag, status)) {
                     ok = false;
                     break;
                 }
                 const uint32_t fb = ptx::smem_addr(&full[stage]);
-                uint8_t* st = base + stage * a.stage_bytes;
-                ptx::mbar_arrive_expect_tx(fb, a.stage_bytes);
+                uint8_t* st = base + stage * stage_bytes;
+                ptx::mbar_arrive_expect_tx(fb, stage_bytes);
                 ptx::tma_load_2d(ptx::smem_addr(st), &a.a, kb * RBK, tile * RBM, fb);
                 ptx::tma_load_2d(ptx::smem_addr(st + RBM * RBK * 2), &a.b, kb * RBK, 0, fb);
                 ++issued;
-                if (++stage == a.stages) {
+                if (++stage == stages) {
                     stage = 0;
                     phase ^= 1;
                 }
             }
             if (!ok) {
-                for (int i = 0; i < issued && i < a.stages; ++i) {
+                for (int i = 0; i < issued && i < stages; ++i) {
                     if (--stage < 0) {
-                        stage = a.stages - 1;
+                        stage = stages - 1;
                         phase ^= 1;
                     }
                     drain_wait(ptx::smem_addr(&full[stage]), phase);
@@ -481,17 +636,17 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
     } else if (warp == 1) {
         // ------------------------------------------------------------------- MMA issuer ----
         if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_bf16_f32(RBM, a.n_pad);
+            const uint32_t idesc = ptx::idesc_bf16_f32(RBM, a.p.n_pad);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true, any = false;
             for (int kb = kb_begin; kb < kb_end; ++kb) {
-                if (!wait_phase(ptx::smem_addr(&full[stage]), phase, abort_flag, a.status)) {
+                if (!wait_phase(ptx::smem_addr(&full[stage]), phase, abort_flag, status)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t a0 = ptx::smem_addr(base + stage * a.stage_bytes);
+                const uint32_t a0 = ptx::smem_addr(base + stage * stage_bytes);
                 const uint32_t b0 = a0 + RBM * RBK * 2;
 #pragma unroll
                 for (int k = 0; k < RBK / 16; ++k)
@@ -500,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
                                  (kb != kb_begin || k != 0) ? 1u : 0u);
                 any = true;
                 ptx::mma_commit(ptx::smem_addr(&empty[stage]));
-                if (++stage == a.stages) {
+                if (++stage == stages) {
                     stage = 0;
                     phase ^= 1;
                 }
@@ -515,72 +670,83 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
         // ------------------------------------------- partial logits of a later K slice ----
         // kept in the idle ring as [n_pad][128] floats for the first CTA of the cluster
         const int quarter = warp & 3;
+        const int n_pad = a.p.n_pad;
         int ok = 1;
-        if (lane == 0) ok = wait_phase(ptx::smem_addr(tfull), 0, abort_flag, a.status);
+        if (lane == 0) ok = wait_phase(ptx::smem_addr(tfull), 0, abort_flag, status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         float* part = reinterpret_cast<float*>(base);
         const int row = quarter * 32 + lane;
+        const int cs = BWD ? n_pad : n_pad >> 2;   // this warp's column slice
+        const int c0 = BWD ? 0 : ((warp - 2) >> 2) * cs;
         if (ok) ptx::tc_fence_after();
-        for (int c = 0; c < a.n_pad / 32; ++c) {
-            uint32_t v[32];
+        for (int c = c0; c < c0 + cs; c += 8) {
+            uint32_t v[8];
             if (ok) {
-                ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
+                ptx::tmem_ld_32x32b_x8(tmem + ((uint32_t)(quarter * 32) << 16) + c, v);
                 ptx::tmem_ld_wait();
             }
 #pragma unroll
-            for (int i = 0; i < 32; ++i)   // zeros if this CTA gave up (its status is set)
-                part[(c * 32 + i) * RBM + row] = ok ? __uint_as_float(v[i]) : 0.f;
+            for (int i = 0; i < 8; ++i)   // zeros if this CTA gave up (its status is set)
+                part[(c + i) * RBM + row] = ok ? __uint_as_float(v[i]) : 0.f;
         }
     }
-    if (a.csize > 1) {   // the partial logits are in place; every thread of the cluster
+    if (csize > 1) {   // the partial logits are in place; every thread of the cluster
         __syncwarp();
         ptx::cluster_sync();
     }
     if (warp >= 2 && leader) {
         // --------------------------------------------------------------------- epilogue ----
+        constexpr int kEpiThreads = router_threads(BWD) - 64;
         const int quarter = warp & 3;
-        const int et = threadIdx.x - 64;   // 0..127 over the four epilogue warps
+        const int et = threadIdx.x - 64;   // 0 .. kEpiThreads-1 over the epilogue warps
         int ok = 1;
-        if (lane == 0) ok = wait_phase(ptx::smem_addr(tfull), 0, abort_flag, a.status);
+        if (lane == 0) ok = wait_phase(ptx::smem_addr(tfull), 0, abort_flag, status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16);
+        // the forward epilogue's barriers need every warp; this barrier also publishes the
+        // scalars' copy
+        ok = epilogue_and<kEpiThreads>(ok);
+        const RouterParams& sp = *ps;
         bool routed_here = false;
         if (ok) {
             ptx::tc_fence_after();
             // the MMAs are complete, so the TMA ring is idle and holds the per-token logit rows
             if constexpr (BWD)
-                route_tile_bwd(a, tb, reinterpret_cast<float*>(base), tile, quarter, lane, colsum,
+                route_tile_bwd(sp, tmem + ((uint32_t)(quarter * 32) << 16),
+                               reinterpret_cast<float*>(base), tile, quarter, lane, colsum,
                                bias_s, aux_s);
             else
-                route_tile<KMAX>(a, tb, reinterpret_cast<float*>(base), tile, quarter, lane,
-                                 colsum, hist, bias_s, chosen);
+                route_tile<KMAX>(sp, tmem, base, tile, warp, lane, colsum, hist, bias_s, chosen,
+                                 chosen_s, red);
             routed_here = true;
         }
         ptx::tc_fence_before();
-        epilogue_bar();
+        epilogue_bar<kEpiThreads>();
         if (routed_here) {
-            for (int j = et; j < N; j += 128) {
+            float* tile_dz = sp.tile_dz;
+            float* tile_psum = sp.tile_psum;
+            int* tile_counts = sp.tile_counts;
+            for (int j = et; j < N; j += kEpiThreads) {
                 const float col = ((colsum[j] + colsum[kMaxRouted + j]) +
                                    colsum[2 * kMaxRouted + j]) + colsum[3 * kMaxRouted + j];
                 if constexpr (BWD) {
-                    a.tile_dz[(size_t)j * n_tiles + tile] = col;
+                    tile_dz[(size_t)j * n_tiles + tile] = col;
                 } else {
-                    a.tile_psum[(size_t)j * n_tiles + tile] = col;
-                    a.tile_counts[(size_t)j * n_tiles + tile] = hist[j];
+                    tile_psum[(size_t)j * n_tiles + tile] = col;
+                    tile_counts[(size_t)j * n_tiles + tile] = hist[j];
                 }
             }
         }
         if constexpr (!BWD) {
-            if (a.fused) finish_single_tile(a, base, hist, colsum, chosen, et, lane);
+            if (sp.fused) finish_single_tile(sp, base, hist, colsum, chosen, et);
         }
     }
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (a.csize > 1) ptx::cluster_sync();   // the first CTA has read the others' partial logits
+    if (csize > 1) ptx::cluster_sync();   // the first CTA has read the others' partial logits
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, a.tmem_cols);
+        ptx::tmem_dealloc(tmem, a.p.tmem_cols);
     }
 }
 
@@ -588,51 +754,58 @@ __global__ void __launch_bounds__(kThreads, 1) router_tc_kernel(const __grid_con
 
 static cudaError_t router_args(const Dims& m, const void* u, const void* centroids,
                                const float* bias, RouterArgs& a) {
-    a.n_pad = router_npad(m);
+    a.p.n_pad = router_npad(m);
     if (!encode_bf16_map(&a.a, u, (uint64_t)m.T, (uint64_t)m.d, RBM) ||
-        !encode_bf16_map(&a.b, centroids, (uint64_t)m.N, (uint64_t)m.d, a.n_pad))
+        !encode_bf16_map(&a.b, centroids, (uint64_t)m.N, (uint64_t)m.d, a.p.n_pad))
         return cudaErrorInvalidValue;
-    a.bias = bias;
-    a.dims = m;
-    a.T = m.T;
-    a.N = m.N;
-    a.K = m.K;
-    a.renorm = m.renorm;
-    a.skip = m.skip;
-    a.k_blocks = m.d / RBK;
-    a.stage_bytes = (uint32_t)(RBM * RBK * 2 + a.n_pad * RBK * 2);
-    a.stages = (int)std::min<uint32_t>(kMaxStages, (192u * 1024u) / a.stage_bytes);
+    a.p.bias = bias;
+    a.p.dims = m;
+    a.p.T = m.T;
+    a.p.N = m.N;
+    a.p.K = m.K;
+    a.p.renorm = m.renorm;
+    a.p.skip = m.skip;
+    a.p.k_blocks = m.d / RBK;
+    a.p.stage_bytes = (uint32_t)(RBM * RBK * 2 + a.p.n_pad * RBK * 2);
+    a.p.stages = (int)std::min<uint32_t>(kMaxStages, (192u * 1024u) / a.p.stage_bytes);
     int cols = 32;
-    while (cols < a.n_pad) cols *= 2;
-    a.tmem_cols = cols;
+    while (cols < a.p.n_pad) cols *= 2;
+    a.p.tmem_cols = cols;
     // few tiles: up to 8 CTAs per tile, while the grid stays within one wave and every CTA keeps
     // at least two K blocks
     const int n_tiles = (m.T + RBM - 1) / RBM;
     int c = 1;
-    while (c < 8 && (long)n_tiles * c * 2 <= sm_count() && a.k_blocks / (c * 2) >= 2) c *= 2;
-    a.csize = c;
+    while (c < 8 && (long)n_tiles * c * 2 <= sm_count() && a.p.k_blocks / (c * 2) >= 2) c *= 2;
+    a.p.csize = c;
     return cudaSuccess;
 }
 
 template <int KMAX, bool BWD>
 static cudaError_t launch_router_kernel(const Dims& m, const RouterArgs& a, cudaStream_t st) {
-    const size_t smem = 1024 + (size_t)a.stages * a.stage_bytes + 8 * (2 * kMaxStages + 2) + 16 +
-                        4 * (4 * kMaxRouted + 3 * kMaxRouted) + 4 * RBM * kMaxTopK;
+    const size_t smem = 1024 + (size_t)a.p.stages * a.p.stage_bytes + 8 * (2 * kMaxStages + 2) + 16 +
+                        4 * (4 * kMaxRouted + 3 * kMaxRouted) + 2 * 4 * RBM * kMaxTopK + 4 * 2 * 4 * RBM +
+                        sizeof(RouterParams);
+    // the forward epilogue keeps the logits [n_pad][128] and the slice lists [4][KMAX][128] (values
+    // and indices) in the idle ring
+    if (!BWD && (size_t)a.p.stages * a.p.stage_bytes <
+                    (size_t)a.p.n_pad * RBM * 4 + (size_t)4 * KMAX * RBM * 8)
+        return cudaErrorInvalidValue;
     const int n_tiles = (m.T + RBM - 1) / RBM;
+    const int threads = router_threads(BWD);
     auto kern = router_tc_kernel<KMAX, BWD>;
     cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    if (a.csize == 1) {
-        e = launch_pdl(kern, dim3(n_tiles), dim3(kThreads), smem, st, a);
+    if (a.p.csize == 1) {
+        e = launch_pdl(kern, dim3(n_tiles), dim3(threads), smem, st, a);
     } else {   // clusters of csize CTAs per tile
         cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(n_tiles * a.csize);
-        cfg.blockDim = dim3(kThreads);
+        cfg.gridDim = dim3(n_tiles * a.p.csize);
+        cfg.blockDim = dim3(threads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)a.csize;
+        attr[0].val.clusterDim.x = (unsigned)a.p.csize;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -653,23 +826,23 @@ cudaError_t launch_router_tc(const Dims& m, const void* u, const void* centroids
     RouterArgs a{};
     cudaError_t e = router_args(m, u, centroids, bias, a);
     if (e != cudaSuccess) return e;
-    a.topk_idx = topk_idx;
-    a.topk_gate = topk_gate;
-    a.tile_counts = tile_counts;
-    a.tile_psum = tile_psum;
-    a.status = status;
+    a.p.topk_idx = topk_idx;
+    a.p.topk_gate = topk_gate;
+    a.p.tile_counts = tile_counts;
+    a.p.tile_psum = tile_psum;
+    a.p.status = status;
     if (tables) {
         if (m.T > RBM) return cudaErrorInvalidValue;   // one tile only
-        a.fused = 1;
-        a.pad = tables->pad;
-        a.counts_out = tables->counts;
-        a.psum_out = tables->psum;
-        a.offsets = tables->offsets;
-        a.perm_token = tables->perm_token;
-        a.perm_slot = tables->perm_slot;
-        a.f_out = tables->f;
-        a.P_out = tables->P;
-        a.losses = tables->losses;
+        a.p.fused = 1;
+        a.p.pad = tables->pad;
+        a.p.counts_out = tables->counts;
+        a.p.psum_out = tables->psum;
+        a.p.offsets = tables->offsets;
+        a.p.perm_token = tables->perm_token;
+        a.p.perm_slot = tables->perm_slot;
+        a.p.f_out = tables->f;
+        a.p.P_out = tables->P;
+        a.p.losses = tables->losses;
     }
     return m.skip + m.K <= 8 ? launch_router_kernel<8, false>(m, a, st)
                              : launch_router_kernel<16, false>(m, a, st);
@@ -683,16 +856,16 @@ cudaError_t launch_router_bwd(const Dims& m, const void* u, const void* centroid
     RouterArgs a{};
     cudaError_t e = router_args(m, u, centroids, bias, a);
     if (e != cudaSuccess) return e;
-    a.topk_idx = const_cast<int*>(topk_idx);
-    a.csize = 1;   // the backward epilogue needs the whole logit row of a token in one CTA
-    a.dgate = dgate;
-    a.counts = counts;
-    a.dz = static_cast<__nv_bfloat16*>(dz);
-    a.tile_dz = tile_dz;
-    a.a1 = m.a1;
-    a.a2 = m.a2;
-    a.D = m.D;
-    a.status = status;
+    a.p.topk_idx = const_cast<int*>(topk_idx);
+    a.p.csize = 1;   // the backward epilogue needs the whole logit row of a token in one CTA
+    a.p.dgate = dgate;
+    a.p.counts = counts;
+    a.p.dz = static_cast<__nv_bfloat16*>(dz);
+    a.p.tile_dz = tile_dz;
+    a.p.a1 = m.a1;
+    a.p.a2 = m.a2;
+    a.p.D = m.D;
+    a.p.status = status;
     return launch_router_kernel<8, true>(m, a, st);
 }
 
