@@ -64,6 +64,23 @@ bool encode_bf16_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t 
            CUDA_SUCCESS;
 }
 
+// Row-major bf16 matrix [rows, cols] as a 3D tensor map over (64-column chunk, row, chunk index)
+// with a box of [chunks x box_rows x 64]: one copy lands `chunks` consecutive [box_rows x 64] tiles,
+// each 128-byte swizzled exactly as a 2D box would be.
+bool encode_bf16_map_chunks(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                            int box_rows, int chunks) {
+    auto fn = tensor_map_encoder();
+    if (!fn || rows == 0 || cols == 0 || cols % 64 != 0) return false;
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)chunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // Row-major bf16 output [rows, cols] with row stride ld (elements) as a 2D TMA map for stores,
 // box [32 rows x box_cols columns] (32: 64-byte rows, 64-byte swizzle; 16: 32-byte rows, 32-byte
 // swizzle); columns >= cols and rows >= rows are clipped.

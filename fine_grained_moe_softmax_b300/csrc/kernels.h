@@ -46,6 +46,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // Row-major bf16 [rows, cols] as a 2D TMA map, box [box_rows x 64], 128-byte swizzle.
 bool encode_bf16_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
                      int box_rows);
+// The same matrix as a 3D map whose box lands `chunks` consecutive [box_rows x 64] swizzled tiles
+// (64-column chunks c, c+1, ...; chunk coordinate = K block index). cols % 64 == 0.
+bool encode_bf16_map_chunks(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols,
+                            int box_rows, int chunks);
 
 // Per-tile histogram of topk_idx (used when the router's tile histogram is not at hand).
 cudaError_t launch_tile_hist(const Dims& m, const int* topk_idx, int* tile_counts, int* status,

@@ -49,6 +49,7 @@ __host__ __device__ constexpr int router_threads(bool bwd) {
 struct RouterParams {
     const float* bias;    // [N'] or null
     int T, N, K, renorm, skip, k_blocks, n_pad, stages, tmem_cols;
+    int kc;               // 64-deep K chunks per stage (one tensor copy each for u and centroids)
     int csize;            // CTAs per tile (cluster size); CTA r takes K blocks [r kb/C, (r+1) kb/C)
     uint32_t stage_bytes;
     int* topk_idx;
@@ -76,8 +77,8 @@ struct RouterParams {
 };
 
 struct RouterArgs {
-    CUtensorMap a;        // u [T, d], box [128 x 64]
-    CUtensorMap b;        // centroids [N', d], box [n_pad x 64]
+    CUtensorMap a;        // u [T, d] in 64-column chunks, box [kc x 128 x 64]
+    CUtensorMap b;        // centroids [N', d] in 64-column chunks, box [kc x n_pad x 64]
     RouterParams p;
 };
 static_assert(sizeof(RouterParams) % 8 == 0, "copied in 4-byte words");
@@ -522,6 +523,7 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // scalars read once into registers (the copy in shared memory serves the epilogue)
     const int stages = a.p.stages, csize = a.p.csize, k_blocks = a.p.k_blocks, N = a.p.N;
+    const int kc = a.p.kc;
     const uint32_t stage_bytes = a.p.stage_bytes;
     int* const status = a.p.status;
     const uint32_t ring = stages * stage_bytes;
@@ -607,16 +609,18 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int kb = kb_begin; kb < kb_end; ++kb) {
+            for (int kb = kb_begin; kb < kb_end; kb += kc) {
                 if (!wait_phase(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag, status)) {
                     ok = false;
                     break;
                 }
+                // the boxes always carry kc chunks (their full bytes count, chunks past d are
+                // zero-filled); the MMAs use only the chunks below kb_end
                 const uint32_t fb = ptx::smem_addr(&full[stage]);
                 uint8_t* st = base + stage * stage_bytes;
                 ptx::mbar_arrive_expect_tx(fb, stage_bytes);
-                ptx::tma_load_2d(ptx::smem_addr(st), &a.a, kb * RBK, tile * RBM, fb);
-                ptx::tma_load_2d(ptx::smem_addr(st + RBM * RBK * 2), &a.b, kb * RBK, 0, fb);
+                ptx::tma_load_3d(ptx::smem_addr(st), &a.a, 0, tile * RBM, kb, fb);
+                ptx::tma_load_3d(ptx::smem_addr(st + kc * RBM * RBK * 2), &a.b, 0, 0, kb, fb);
                 ++issued;
                 if (++stage == stages) {
                     stage = 0;
@@ -640,19 +644,24 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true, any = false;
-            for (int kb = kb_begin; kb < kb_end; ++kb) {
+            const uint32_t b_chunk = (uint32_t)a.p.n_pad * RBK * 2;
+            for (int kb = kb_begin; kb < kb_end; kb += kc) {
                 if (!wait_phase(ptx::smem_addr(&full[stage]), phase, abort_flag, status)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t a0 = ptx::smem_addr(base + stage * stage_bytes);
-                const uint32_t b0 = a0 + RBM * RBK * 2;
+                const uint32_t b0 = a0 + kc * RBM * RBK * 2;
+                const int nc = min(kc, kb_end - kb);
+                for (int c = 0; c < nc; ++c) {
+                    const uint32_t ac = a0 + c * RBM * RBK * 2, bc = b0 + c * b_chunk;
 #pragma unroll
-                for (int k = 0; k < RBK / 16; ++k)
-                    ptx::mma_f16(tmem, ptx::sw128_kmajor_desc(a0 + k * 32),
-                                 ptx::sw128_kmajor_desc(b0 + k * 32), idesc,
-                                 (kb != kb_begin || k != 0) ? 1u : 0u);
+                    for (int k = 0; k < RBK / 16; ++k)
+                        ptx::mma_f16(tmem, ptx::sw128_kmajor_desc(ac + k * 32),
+                                     ptx::sw128_kmajor_desc(bc + k * 32), idesc,
+                                     (kb != kb_begin || c != 0 || k != 0) ? 1u : 0u);
+                }
                 any = true;
                 ptx::mma_commit(ptx::smem_addr(&empty[stage]));
                 if (++stage == stages) {
@@ -755,8 +764,12 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
 static cudaError_t router_args(const Dims& m, const void* u, const void* centroids,
                                const float* bias, RouterArgs& a) {
     a.p.n_pad = router_npad(m);
-    if (!encode_bf16_map(&a.a, u, (uint64_t)m.T, (uint64_t)m.d, RBM) ||
-        !encode_bf16_map(&a.b, centroids, (uint64_t)m.N, (uint64_t)m.d, a.p.n_pad))
+    // a stage of up to 96 KB: kc 64-deep chunks of the u tile and of the centroids, each loaded by
+    // one tensor copy (the ring keeps at least two stages)
+    const uint32_t chunk_bytes = (uint32_t)(RBM * RBK * 2 + a.p.n_pad * RBK * 2);
+    a.p.kc = (int)std::max<uint32_t>(1u, std::min<uint32_t>(4u, (96u * 1024u) / chunk_bytes));
+    if (!encode_bf16_map_chunks(&a.a, u, (uint64_t)m.T, (uint64_t)m.d, RBM, a.p.kc) ||
+        !encode_bf16_map_chunks(&a.b, centroids, (uint64_t)m.N, (uint64_t)m.d, a.p.n_pad, a.p.kc))
         return cudaErrorInvalidValue;
     a.p.bias = bias;
     a.p.dims = m;
@@ -766,7 +779,7 @@ static cudaError_t router_args(const Dims& m, const void* u, const void* centroi
     a.p.renorm = m.renorm;
     a.p.skip = m.skip;
     a.p.k_blocks = m.d / RBK;
-    a.p.stage_bytes = (uint32_t)(RBM * RBK * 2 + a.p.n_pad * RBK * 2);
+    a.p.stage_bytes = chunk_bytes * (uint32_t)a.p.kc;
     a.p.stages = (int)std::min<uint32_t>(kMaxStages, (192u * 1024u) / a.p.stage_bytes);
     int cols = 32;
     while (cols < a.p.n_pad) cols *= 2;

@@ -108,6 +108,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 3D tiled load of the box at (x, y, z) into shared memory (see encode_bf16_map_chunks); completion
+// counted in bytes on `bar`, out-of-range elements filled with zeros.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 // 2D tiled load by one CTA of a CTA pair: the box lands in this CTA's shared memory and its
 // bytes are counted on `cluster_bar`, an mbarrier of either CTA of the pair (shared::cluster
 // address).
