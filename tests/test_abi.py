@@ -115,3 +115,31 @@ def test_profile_read_without_calls(lib):
                                         ctypes.byref(n_split)) == 0
     assert n.value == 0 and n_split.value == 0 and gu.value == 0.0
     assert lib.moe_profile_read_gate_up(None, ctypes.byref(n), ctypes.byref(n_split)) == -1
+
+
+def test_layer_routing_views_stay_inside_the_workspace(lib):
+    """moe_layer_routing only hands out pointers into the caller's workspace (nothing is
+    dereferenced, so a fake aligned address stands in for device memory): the four tables lie
+    inside [ws, ws + moe_workspace_bytes), do not overlap, are 256-byte aligned, and have room for
+    their sizes. NULL outputs are allowed; a bad config or workspace is refused."""
+    P = ctypes.c_void_p
+    for sh in (moe_inputs.CONFIGS["16b_bf16"], moe_inputs.CONFIGS["tiny_f32"]):
+        cfg = B.MoEConfig.from_shape(sh)
+        base, nbytes = 1 << 30, lib.moe_workspace_bytes(ctypes.byref(cfg))
+        out = [P() for _ in range(4)]
+        assert lib.moe_layer_routing(ctypes.byref(cfg), P(base), nbytes,
+                                     *[ctypes.byref(p) for p in out]) == 0
+        TK, N = sh.T * sh.top_k, sh.n_routed
+        spans = sorted((p.value, p.value + 4 * n) for p, n in zip(out, (N + 1, TK, TK, N)))
+        for lo, hi in spans:
+            assert base <= lo and hi <= base + nbytes and lo % 256 == 0
+        for (lo1, hi1), (lo2, _) in zip(spans, spans[1:]):
+            assert hi1 <= lo2
+        assert lib.moe_layer_routing(ctypes.byref(cfg), P(base), nbytes, None, None, None,
+                                     None) == 0
+        assert lib.moe_layer_routing(ctypes.byref(cfg), P(base), nbytes - 1,
+                                     *[ctypes.byref(p) for p in out]) == -3
+        assert lib.moe_layer_routing(ctypes.byref(cfg), P(base + 16), nbytes,
+                                     *[ctypes.byref(p) for p in out]) == -3
+    assert lib.moe_layer_routing(ctypes.byref(_cfg(top_k=9)), P(1 << 30), 1 << 30, None, None,
+                                 None, None) == -1
