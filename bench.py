@@ -449,7 +449,8 @@ def dominant_roofline(sh, T, counts, gu_launch_ms, n_prof, n_split) -> dict:
 
 # Workloads timed beside the headline in the default run: (name, CUDA-graph replay).
 PER_CONFIG = [("2b_bf16", False), ("145b_zipf_bf16", False), ("16b_decode_bf16", False),
-              ("16b_decode_bf16", True)]
+              ("16b_decode_bf16", True), ("2b_half_activated_bf16", False),
+              ("2b_gshard_top2_bf16", False)]
 
 
 def measure_workload(name, graph, steps, warmup, dev) -> dict:
