@@ -104,6 +104,12 @@ def _custom(**kw):
     dict(d=128, inter=320, T=200),                  # 160-column gate/up tiles
     dict(d=256, inter=128, T=40),                   # <= 64 tokens: 64-row A tiles, 5 stages
     dict(n_routed=256, top_k=8, n_groups=8, T=300), # widest router
+    # router column slices with ragged ends (n_pad 224, 128, 64 over 200, 100, 40 experts), stages
+    # of 2, 3 and 4 K chunks with a shorter last stage, one-tile and cluster-split tiles
+    dict(n_routed=200, top_k=8, n_groups=8, d=640, T=300),
+    dict(n_routed=100, top_k=5, n_groups=4, d=512, T=64),
+    dict(n_routed=40, top_k=6, n_groups=5, d=1152, T=64, renormalize=1),
+    dict(n_routed=40, top_k=6, n_groups=5, d=1152, T=700),
     # 75 MB of shared gate/up weights: column panels of the shared group, the last one narrower
     dict(d=2048, n_shared=9, inter=1024, T=300),
     dict(dtype="f32", renormalize=1, n_shared=2),
