@@ -7,7 +7,9 @@
 //
 // The logits of a 128-token tile are one [128 x d] x [d x N'] product: the tile's token rows and
 // the centroids stream through a TMA ring into tcgen05.mma (M = 128, N = N' rounded up to 32),
-// accumulating fp32 logits in TMEM. When there are few tiles (decode-sized batches), a cluster of
+// accumulating fp32 logits in TMEM. A ring stage holds up to four 64-deep K chunks, and each
+// operand of a stage is one 3D tensor copy (a copy costs about the same whatever its size, so
+// fewer, larger copies move more bytes per cycle). When there are few tiles (decode-sized batches), a cluster of
 // C CTAs shares a tile, each over 1/C of d; the other CTAs leave their partial logits in their
 // shared memory and the first adds them to its own, in rank order, through distributed shared
 // memory, so the sum does not depend on timing.
