@@ -80,6 +80,11 @@ cudaError_t launch_perm_scatter(const Dims& m, const int* topk_idx, const int* o
                                 cudaStream_t st);
 
 // x_perm[perm_slot[t*K+k]] = u[t]; rows outside [0, row_limit) (default T*K') are corrupt.
+// The layer call's gather, which also places the assignments: perm_slot / perm_token as
+// perm_scatter_kernel writes them, from the finalize kernel's offsets and per-tile bases.
+cudaError_t launch_gather_place(const Dims& m, const void* u, const int* topk_idx,
+                                const int* offsets, const int* tile_base, int* perm_token,
+                                int* perm_slot, void* x_perm, int* status, cudaStream_t st);
 cudaError_t launch_gather(const Dims& m, const void* u, const int* perm_slot, void* x_perm,
                           int* status, cudaStream_t st, long row_limit = 0);
 

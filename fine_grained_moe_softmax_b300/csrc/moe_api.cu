@@ -366,14 +366,14 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
         fa.status = status;
         e = launch_route_finalize(fa, st);
     }
-    if (e == cudaSuccess && !one_tile)
-        e = launch_perm_scatter(m, topk_idx, offsets, tb, perm_token, perm_slot, st);
     mk.mark(2);
     // With shared experts, the shared group's gate/up GEMM needs only u. The permuted token rows
-    // are then gathered on a side stream while it runs (the gather needs no shared memory, so its
-    // CTAs fit beside the GEMM's, and the GEMM leaves most of the memory bandwidth idle); the
-    // routed groups' gate/up follows once they are ready. The gather stage of the profile is then
-    // timed on the side stream and the gate/up stage is the rest of the gate/up work.
+    // are then placed and gathered on a side stream while it runs (the gather needs no shared
+    // memory, so its CTAs fit beside the GEMM's, and the GEMM leaves most of the memory bandwidth
+    // idle); the routed groups' gate/up follows once they are ready. The gather stage of the
+    // profile is then timed on the side stream and the gate/up stage is the rest of the gate/up
+    // work. Several tiles: the gather also computes perm_slot / perm_token (the scatter kernel's
+    // results) from the finalize kernel's offsets and tile bases; one tile: the router wrote them.
     const bool overlap = e == cudaSuccess && !one_tile && m.dtype == MOE_DTYPE_BF16 &&
                          m.shared_active();
     SideStream* ss = nullptr;
@@ -386,7 +386,10 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
         if ((e = cudaEventRecord(ss->fork, st)) == cudaSuccess)
             e = cudaStreamWaitEvent(sst, ss->fork, 0);
     }
-    if (e == cudaSuccess) e = launch_gather(m, u, perm_slot, at<void>(ws, L.x_perm), status, sst);
+    if (e == cudaSuccess)
+        e = one_tile ? launch_gather(m, u, perm_slot, at<void>(ws, L.x_perm), status, sst)
+                     : launch_gather_place(m, u, topk_idx, offsets, tb, perm_token, perm_slot,
+                                           at<void>(ws, L.x_perm), status, sst);
     mk.mark_on(3, sst);
     bool joined = !overlap;
     if (overlap) {

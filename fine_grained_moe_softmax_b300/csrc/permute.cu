@@ -217,6 +217,178 @@ __global__ void gather_cta_kernel(Dims m, const uint4* __restrict__ u,
     }
 }
 
+// The rows of token t's assignments, by one warp, for the layer call's gather (which so takes over
+// the work of perm_scatter_kernel, off the path that the shared experts' GEMM waits for). With
+// b = t / 128, the row of (t, k) is offsets[j] + tile_base[j][b] + the number of assignments of
+// the tile's earlier tokens to j = topk_idx[t][k]: a token chooses an expert at most once and
+// assignments are ordered token-major, so these are the rows of perm_scatter_kernel's counting
+// sort, bit for bit. rows[k] = -1 (and `bad`) for an expert id or a row out of range.
+template <int KB>
+__device__ __forceinline__ void place_token(const Dims& m, int t, const int* __restrict__ topk_idx,
+                                            const int* __restrict__ offsets,
+                                            const int* __restrict__ tile_base, int n_tiles,
+                                            long TK, int lane, int (&rows)[KB], bool& bad) {
+    const int K = m.K, N = m.N;
+    const int tile = t / kRouteTile;
+    int j[KB], cnt[KB];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+        j[k] = k < K ? topk_idx[(size_t)t * K + k] : -1;
+        cnt[k] = 0;
+    }
+    for (long a = (long)tile * kRouteTile * K + lane; a < (long)t * K; a += 32) {
+        const int x = topk_idx[a];
+#pragma unroll
+        for (int k = 0; k < KB; ++k) cnt[k] += (x == j[k]) ? 1 : 0;
+    }
+    bad = false;
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+        const int c = __reduce_add_sync(0xffffffffu, cnt[k]);
+        rows[k] = -1;
+        if (k < K) {
+            if (j[k] >= 0 && j[k] < N) {
+                const long r = (long)offsets[j[k]] + tile_base[(size_t)j[k] * n_tiles + tile] + c;
+                if (r >= 0 && r < TK) rows[k] = (int)r;
+                else bad = true;
+            } else {
+                bad = true;
+            }
+        }
+    }
+}
+
+// Writes the token's perm_slot entries and the perm_token entries of its rows.
+template <int KB>
+__device__ __forceinline__ void write_places(const Dims& m, int t, const int (&rows)[KB], int lane,
+                                             int* __restrict__ perm_token,
+                                             int* __restrict__ perm_slot) {
+#pragma unroll
+    for (int k = 0; k < KB; ++k)
+        if (k < m.K && lane == k) {
+            perm_slot[(size_t)t * m.K + k] = rows[k];
+            if (rows[k] >= 0) perm_token[rows[k]] = t;
+        }
+}
+
+// Gather with placement, one warp per token and eight tokens per CTA (a CTA's tokens lie in one
+// 128-token tile). The CTA first counts, per expert, the assignments of the tile's tokens before
+// its own (shared-memory histogram); warp w then adds the assignments of the CTA's tokens before
+// token w to its experts, which gives the rows of place_token. The token's row is read once
+// (16-byte vectors; its first 4 KB before the placement, so that the loads overlap it) and
+// written to its K' rows.
+template <int KB>
+__global__ void __launch_bounds__(256) gather_place_kernel(
+    Dims m, const uint4* __restrict__ u, const int* __restrict__ topk_idx,
+    const int* __restrict__ offsets, const int* __restrict__ tile_base, int n_tiles,
+    int* __restrict__ perm_token, int* __restrict__ perm_slot, uint4* __restrict__ x_perm,
+    int* status, long TK) {
+    static_assert(kRouteTile % 8 == 0, "a CTA's eight tokens lie in one tile");
+    __shared__ int hist[kMaxRouted];
+    pdl_wait();
+    pdl_trigger();
+    const int K = m.K, N = m.N;
+    const int t0 = blockIdx.x * 8, lane = threadIdx.x & 31;
+    const int tile = t0 / kRouteTile;
+    const int t = t0 + (threadIdx.x >> 5);
+    const int vec_per_row = m.d * m.elem() / 16;
+    constexpr int kHead = 8;   // 16-byte vectors per lane loaded before the placement
+    uint4 head[kHead];
+    if (t < m.T) {
+#pragma unroll
+        for (int i = 0; i < kHead; ++i)
+            if (lane + 32 * i < vec_per_row) head[i] = u[(size_t)t * vec_per_row + lane + 32 * i];
+    }
+    for (int j = threadIdx.x; j < N; j += blockDim.x) hist[j] = 0;
+    __syncthreads();
+    for (long a = (long)tile * kRouteTile * K + threadIdx.x; a < (long)t0 * K; a += blockDim.x) {
+        const int x = topk_idx[a];
+        if (x >= 0 && x < N) atomicAdd(&hist[x], 1);
+    }
+    __syncthreads();
+    if (t >= m.T) return;
+    int j[KB], cnt[KB];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+        j[k] = k < K ? topk_idx[(size_t)t * K + k] : -1;
+        cnt[k] = 0;
+    }
+    for (long a = (long)t0 * K + lane; a < (long)t * K; a += 32) {   // at most 7 K' entries
+        const int x = topk_idx[a];
+#pragma unroll
+        for (int k = 0; k < KB; ++k) cnt[k] += (x == j[k]) ? 1 : 0;
+    }
+    int rows[KB];
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+        const int c = __reduce_add_sync(0xffffffffu, cnt[k]);
+        rows[k] = -1;
+        if (k < K) {
+            if (j[k] >= 0 && j[k] < N) {
+                const long r = (long)offsets[j[k]] + tile_base[(size_t)j[k] * n_tiles + tile] +
+                               hist[j[k]] + c;
+                if (r >= 0 && r < TK) rows[k] = (int)r;
+                else bad = true;
+            } else {
+                bad = true;
+            }
+        }
+    }
+    if (bad && lane == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
+    write_places<KB>(m, t, rows, lane, perm_token, perm_slot);
+#pragma unroll
+    for (int i = 0; i < kHead; ++i) {
+        const int v = lane + 32 * i;
+        if (v < vec_per_row) {
+#pragma unroll
+            for (int k = 0; k < KB; ++k)
+                if (k < K && rows[k] >= 0) x_perm[(size_t)rows[k] * vec_per_row + v] = head[i];
+        }
+    }
+    for (int v = lane + 32 * kHead; v < vec_per_row; v += 32) {
+        const uint4 x = u[(size_t)t * vec_per_row + v];
+#pragma unroll
+        for (int k = 0; k < KB; ++k)
+            if (k < K && rows[k] >= 0) x_perm[(size_t)rows[k] * vec_per_row + v] = x;
+    }
+}
+
+// The same for small batches, one CTA per token: warp 0 places the token, every thread copies.
+template <int KB>
+__global__ void gather_place_cta_kernel(Dims m, const uint4* __restrict__ u,
+                                        const int* __restrict__ topk_idx,
+                                        const int* __restrict__ offsets,
+                                        const int* __restrict__ tile_base, int n_tiles,
+                                        int* __restrict__ perm_token, int* __restrict__ perm_slot,
+                                        uint4* __restrict__ x_perm, int* status, long TK) {
+    __shared__ int rows_s[KB];
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x, lane = threadIdx.x & 31;
+    if (threadIdx.x < 32) {
+        int rows[KB];
+        bool bad;
+        place_token<KB>(m, t, topk_idx, offsets, tile_base, n_tiles, TK, lane, rows, bad);
+        if (bad && lane == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
+        write_places<KB>(m, t, rows, lane, perm_token, perm_slot);
+#pragma unroll
+        for (int k = 0; k < KB; ++k)
+            if (lane == k) rows_s[k] = rows[k];
+    }
+    __syncthreads();
+    int rows[KB];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) rows[k] = k < m.K ? rows_s[k] : -1;
+    const int vec_per_row = m.d * m.elem() / 16;
+    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
+        const uint4 x = u[(size_t)t * vec_per_row + v];
+#pragma unroll
+        for (int k = 0; k < KB; ++k)
+            if (k < m.K && rows[k] >= 0) x_perm[(size_t)rows[k] * vec_per_row + v] = x;
+    }
+}
+
 // One warp per permuted row: x_perm[r] = u[perm_token[r]] for the rows the offsets cover.
 __global__ void gather_rows_kernel(Dims m, const uint4* __restrict__ u,
                                    const int* __restrict__ offsets,
@@ -303,6 +475,46 @@ cudaError_t launch_gather(const Dims& m, const void* u, const int* perm_slot, vo
                        static_cast<const uint4*>(u), perm_slot, static_cast<uint4*>(x_perm), status,
                        rows);
     }
+    if (e != cudaSuccess) return e;
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+template <int KB>
+static cudaError_t launch_gather_place_kb(const Dims& m, const void* u, const int* topk_idx,
+                                          const int* offsets, const int* tile_base,
+                                          int* perm_token, int* perm_slot, void* x_perm,
+                                          int* status, cudaStream_t st) {
+    const int n_tiles = (m.T + kRouteTile - 1) / kRouteTile;
+    const long TK = (long)m.T * m.K;
+    if (m.T <= 2 * sm_count()) {   // a warp per token would leave most SMs idle
+        const int vecs = m.d * m.elem() / 16;
+        const int tpb = vecs >= 256 ? 256 : ((vecs + 31) / 32) * 32;
+        return launch_pdl(gather_place_cta_kernel<KB>, dim3(m.T), dim3(tpb), 0, st, m,
+                          static_cast<const uint4*>(u), topk_idx, offsets, tile_base, n_tiles,
+                          perm_token, perm_slot, static_cast<uint4*>(x_perm), status, TK);
+    }
+    const int threads = 256, warps_per_block = threads / 32;
+    const int blocks = (m.T + warps_per_block - 1) / warps_per_block;
+    return launch_pdl(gather_place_kernel<KB>, dim3(blocks), dim3(threads), 0, st, m,
+                      static_cast<const uint4*>(u), topk_idx, offsets, tile_base, n_tiles,
+                      perm_token, perm_slot, static_cast<uint4*>(x_perm), status, TK);
+}
+
+cudaError_t launch_gather_place(const Dims& m, const void* u, const int* topk_idx,
+                                const int* offsets, const int* tile_base, int* perm_token,
+                                int* perm_slot, void* x_perm, int* status, cudaStream_t st) {
+    if (m.T == 0) return cudaSuccess;
+    cudaError_t e;
+    if (m.K <= 4)
+        e = launch_gather_place_kb<4>(m, u, topk_idx, offsets, tile_base, perm_token, perm_slot,
+                                      x_perm, status, st);
+    else if (m.K <= 8)
+        e = launch_gather_place_kb<8>(m, u, topk_idx, offsets, tile_base, perm_token, perm_slot,
+                                      x_perm, status, st);
+    else
+        e = launch_gather_place_kb<kMaxTopK>(m, u, topk_idx, offsets, tile_base, perm_token,
+                                             perm_slot, x_perm, status, st);
     if (e != cudaSuccess) return e;
     note_launches(1);
     return cudaGetLastError();

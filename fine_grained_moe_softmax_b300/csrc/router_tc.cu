@@ -200,10 +200,13 @@ __device__ __noinline__ void finish_single_tile(const RouterParams& a, uint8_t* 
     float* ptot = reinterpret_cast<float*>(off + kMaxRouted + 1);   // [N']
     float* fs = ptot + kMaxRouted;                                  // [N']
     float* Ps = fs + kMaxRouted;                                    // [N']
+    int* seg = reinterpret_cast<int*>(Ps + kMaxRouted);             // [N']: padded segment rows
+    const int pad = a.pad;
     for (int i = et; i < 4 * N; i += kEpiThreadsFwd) bits[i] = 0u;
     for (int j = et; j < N; j += kEpiThreadsFwd) {
         const float col = ((colsum[j] + colsum[kMaxRouted + j]) + colsum[2 * kMaxRouted + j]) +
                           colsum[3 * kMaxRouted + j];
+        seg[j] = pad > 0 ? (hist[j] + pad - 1) / pad * pad : hist[j];
         ptot[j] = col;
         a.counts_out[j] = hist[j];
         a.psum_out[j] = col;
@@ -215,11 +218,9 @@ __device__ __noinline__ void finish_single_tile(const RouterParams& a, uint8_t* 
         if (j >= 0 && j < N) atomicOr(&bits[j * 4 + (t >> 5)], 1u << (t & 31));
     }
     if (et < 32) {   // offsets: lane l scans experts 8l .. 8l+7 (N' <= 256)
-        const int pad = a.pad;
         int sum = 0;
 #pragma unroll 1
-        for (int j = lane * 8; j < min(lane * 8 + 8, N); ++j)
-            sum += pad > 0 ? (hist[j] + pad - 1) / pad * pad : hist[j];
+        for (int j = lane * 8; j < min(lane * 8 + 8, N); ++j) sum += seg[j];
         int incl = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -230,13 +231,14 @@ __device__ __noinline__ void finish_single_tile(const RouterParams& a, uint8_t* 
 #pragma unroll 1
         for (int j = lane * 8; j < min(lane * 8 + 8, N); ++j) {
             off[j] = run;
-            run += pad > 0 ? (hist[j] + pad - 1) / pad * pad : hist[j];
+            run += seg[j];
         }
         if (lane == 31) off[N] = incl;
-    } else if (et < 64 && a.losses) {
-        balance_losses_warp(a.dims, fs, Ps, a.losses, lane);
     }
     epilogue_bar<kEpiThreadsFwd>();
+    // the balance losses by the last warp, beside the permutation below (a decode-sized batch
+    // leaves that warp without permutation entries)
+    if (et >= kEpiThreadsFwd - 32 && a.losses) balance_losses_warp(a.dims, fs, Ps, a.losses, lane);
     for (int j = et; j <= N; j += kEpiThreadsFwd) a.offsets[j] = off[j];
     if (a.f_out)
         for (int j = et; j < N; j += kEpiThreadsFwd) {
@@ -261,10 +263,10 @@ __device__ __noinline__ void finish_single_tile(const RouterParams& a, uint8_t* 
 // at j * 128 + r, conflict-free per warp), then the slice lists [4][KMAX][128] (values, then
 // indices); `red` holds the slices' maxima and exponential sums [2][4][128].
 template <int KMAX>
-__device__ __forceinline__ void route_tile(const RouterParams& a, uint32_t tmem, uint8_t* ring,
-                                          int tile, int warp, int lane, float* colsum, int* hist,
-                                          const float* bias_s, int* chosen, float* chosen_s,
-                                          float* red) {
+__device__ __noinline__ void route_tile(const RouterParams& a, uint32_t tmem, uint8_t* ring,
+                                        int tile, int warp, int lane, float* colsum, int* hist,
+                                        const float* bias_s, int* chosen, float* chosen_s,
+                                        float* red) {
     const int N = a.N, K = a.K;
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int row = q * 32 + lane;
@@ -280,6 +282,9 @@ __device__ __forceinline__ void route_tile(const RouterParams& a, uint32_t tmem,
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     // the other CTAs of the cluster keep their partial logits at the same offset as zc
     const uint32_t part = ptx::smem_addr(zc);
+    // a warp whose 32 rows are all past the batch (in a tile of at most 96 tokens) skips phases
+    // A, B and D and contributes zero column sums, leaving the issue slots to the warps with tokens
+    const bool qvalid = q * 32 < rows_valid;
 
     // A: the slice's biased logits, their maximum and the slice's top list. The epilogue runs once
     // per launch, so its code is fetched cold: loops stay rolled where unrolling buys nothing.
@@ -287,7 +292,7 @@ __device__ __forceinline__ void route_tile(const RouterParams& a, uint32_t tmem,
     TopK<KMAX> top;
     top.init();
 #pragma unroll 1
-    for (int c = c0; c < c0 + cs; c += 8) {
+    for (int c = c0; c < (qvalid ? c0 + cs : c0); c += 8) {
         uint32_t v[8];
         ptx::tmem_ld_32x32b_x8(tl + c, v);
         ptx::tmem_ld_wait();
@@ -338,7 +343,7 @@ __device__ __forceinline__ void route_tile(const RouterParams& a, uint32_t tmem,
     const float zmax = fmaxf(fmaxf(red_max[row], red_max[RBM + row]),
                              fmaxf(red_max[2 * RBM + row], red_max[3 * RBM + row]));
     float ssum = 0.f;
-    const int c1 = min(c0 + cs, N);
+    const int c1 = qvalid ? min(c0 + cs, N) : c0;
     for (int j = c0; j < c1; ++j) {
         const float e = __expf(zc[j * RBM + row] - zmax);
         zc[j * RBM + row] = e;
@@ -378,7 +383,7 @@ __device__ __forceinline__ void route_tile(const RouterParams& a, uint32_t tmem,
         float gsum = 0.f;
         bool bad = !(zm < INFINITY);
 #pragma unroll 1
-        for (int r = 0; r < q0 + K; ++r) {
+        for (int r = 0; r < (qvalid ? q0 + K : 0); ++r) {
             float v = p < KMAX ? lv[(sub * KMAX + p) * RBM + tr] : -INFINITY;
             int ix = p < KMAX ? li[(sub * KMAX + p) * RBM + tr] : -1;
             int sl = sub;
@@ -578,27 +583,6 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
     }
     pdl_wait();
     pdl_trigger();
-    {
-        const float* bias = a.p.bias;
-        for (int j = threadIdx.x; j < kMaxRouted; j += blockDim.x)
-            bias_s[j] = (bias && j < N) ? bias[j] : 0.f;
-    }
-    if constexpr (BWD) {   // balance-loss gradient per expert: (a1 f_j + a2 f'_group(j)) / T
-        const int* counts = a.p.counts;
-        const int K = a.p.K, D = a.p.D;
-        const float Tf = (float)a.p.T, scale = (float)N / ((float)K * Tf);
-        const float a1 = a.p.a1, a2 = a.p.a2;
-        const int gbase = N / D, extra = N % D;
-        for (int j = threadIdx.x; j < N; j += blockDim.x) {
-            const int g = j < extra * (gbase + 1) ? j / (gbase + 1)
-                                                  : extra + (j - extra * (gbase + 1)) / gbase;
-            const int first = g * gbase + (g < extra ? g : extra);
-            const int size = gbase + (g < extra ? 1 : 0);
-            float fs = 0.f;
-            for (int q = first; q < first + size; ++q) fs += scale * (float)counts[q];
-            aux_s[j] = (a1 * scale * (float)counts[j] + a2 * fs / (float)size) / Tf;
-        }
-    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -700,10 +684,38 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
             for (int i = 0; i < 8; ++i)   // zeros if this CTA gave up (its status is set)
                 part[(c + i) * RBM + row] = ok ? __uint_as_float(v[i]) : 0.f;
         }
+    } else {
+        // the first CTA's epilogue warps: per-expert inputs of the epilogue, read while the K loop
+        // runs (off the producer's path; the epilogue's first barrier publishes them)
+        constexpr int kEpi = router_threads(BWD) - 64;
+        const int et = threadIdx.x - 64;
+        {
+            const float* bias = a.p.bias;
+            for (int j = et; j < kMaxRouted; j += kEpi)
+                bias_s[j] = (bias && j < N) ? bias[j] : 0.f;
+        }
+        if constexpr (BWD) {   // balance-loss gradient per expert: (a1 f_j + a2 f'_group(j)) / T
+            const int* counts = a.p.counts;
+            const int K = a.p.K, D = a.p.D;
+            const float Tf = (float)a.p.T, scale = (float)N / ((float)K * Tf);
+            const float a1 = a.p.a1, a2 = a.p.a2;
+            const int gbase = N / D, extra = N % D;
+            for (int j = et; j < N; j += kEpi) {
+                const int g = j < extra * (gbase + 1) ? j / (gbase + 1)
+                                                      : extra + (j - extra * (gbase + 1)) / gbase;
+                const int first = g * gbase + (g < extra ? g : extra);
+                const int size = gbase + (g < extra ? 1 : 0);
+                float fs = 0.f;
+                for (int q = first; q < first + size; ++q) fs += scale * (float)counts[q];
+                aux_s[j] = (a1 * scale * (float)counts[j] + a2 * fs / (float)size) / Tf;
+            }
+        }
     }
     if (csize > 1) {   // the partial logits are in place; every thread of the cluster
         __syncwarp();
         ptx::cluster_sync();
+        // the first CTA's producer and MMA warps read no partial logits
+        if (leader && warp < 2) ptx::cluster_arrive();
     }
     if (warp >= 2 && leader) {
         // --------------------------------------------------------------------- epilogue ----
@@ -714,7 +726,7 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
         if (lane == 0) ok = wait_phase(ptx::smem_addr(tfull), 0, abort_flag, status);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         // the forward epilogue's barriers need every warp; this barrier also publishes the
-        // scalars' copy
+        // scalars' copy and the per-expert inputs
         ok = epilogue_and<kEpiThreads>(ok);
         const RouterParams& sp = *ps;
         bool routed_here = false;
@@ -729,6 +741,10 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
                 route_tile<KMAX>(sp, tmem, base, tile, warp, lane, colsum, hist, bias_s, chosen,
                                  chosen_s, red);
             routed_here = true;
+        }
+        if (csize > 1) {   // this thread has read its share of the partial logits
+            __syncwarp();
+            ptx::cluster_arrive();
         }
         ptx::tc_fence_before();
         epilogue_bar<kEpiThreads>();
@@ -754,7 +770,12 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (csize > 1) ptx::cluster_sync();   // the first CTA has read the others' partial logits
+    if (csize > 1) {
+        // the first CTA's threads arrived once they had read the others' partial logits; the
+        // other CTAs keep their shared memory until then
+        if (!leader) ptx::cluster_arrive();
+        ptx::cluster_wait();
+    }
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, a.p.tmem_cols);
