@@ -274,9 +274,9 @@ __device__ __forceinline__ void write_places(const Dims& m, int t, const int (&r
 // Gather with placement, one warp per token and eight tokens per CTA (a CTA's tokens lie in one
 // 128-token tile). The CTA first counts, per expert, the assignments of the tile's tokens before
 // its own (shared-memory histogram); warp w then adds the assignments of the CTA's tokens before
-// token w to its experts, which gives the rows of place_token. The token's row is read once
-// (16-byte vectors; its first 4 KB before the placement, so that the loads overlap it) and
-// written to its K' rows.
+// token w to its experts, which gives the rows of place_token. The loads that do not depend on
+// the histogram (the token's experts and the first rows of their segments in this tile) are issued
+// before it. The token's row is then read once (16-byte vectors) and written to its K' rows.
 template <int KB>
 __global__ void __launch_bounds__(256) gather_place_kernel(
     Dims m, const uint4* __restrict__ u, const int* __restrict__ topk_idx,
@@ -291,15 +291,23 @@ __global__ void __launch_bounds__(256) gather_place_kernel(
     const int t0 = blockIdx.x * 8, lane = threadIdx.x & 31;
     const int tile = t0 / kRouteTile;
     const int t = t0 + (threadIdx.x >> 5);
-    const int vec_per_row = m.d * m.elem() / 16;
-    constexpr int kHead = 8;   // 16-byte vectors per lane loaded before the placement
-    uint4 head[kHead];
+    int j[KB];
+    long seg0[KB];
+#pragma unroll
+    for (int k = 0; k < KB; ++k) {
+        j[k] = -1;
+        seg0[k] = -1;
+    }
     if (t < m.T) {
 #pragma unroll
-        for (int i = 0; i < kHead; ++i)
-            if (lane + 32 * i < vec_per_row) head[i] = u[(size_t)t * vec_per_row + lane + 32 * i];
+        for (int k = 0; k < KB; ++k)
+            if (k < K) j[k] = topk_idx[(size_t)t * K + k];
+#pragma unroll
+        for (int k = 0; k < KB; ++k)
+            if (k < K && j[k] >= 0 && j[k] < N)
+                seg0[k] = (long)offsets[j[k]] + tile_base[(size_t)j[k] * n_tiles + tile];
     }
-    for (int j = threadIdx.x; j < N; j += blockDim.x) hist[j] = 0;
+    for (int q = threadIdx.x; q < N; q += blockDim.x) hist[q] = 0;
     __syncthreads();
     for (long a = (long)tile * kRouteTile * K + threadIdx.x; a < (long)t0 * K; a += blockDim.x) {
         const int x = topk_idx[a];
@@ -307,12 +315,9 @@ __global__ void __launch_bounds__(256) gather_place_kernel(
     }
     __syncthreads();
     if (t >= m.T) return;
-    int j[KB], cnt[KB];
+    int cnt[KB];
 #pragma unroll
-    for (int k = 0; k < KB; ++k) {
-        j[k] = k < K ? topk_idx[(size_t)t * K + k] : -1;
-        cnt[k] = 0;
-    }
+    for (int k = 0; k < KB; ++k) cnt[k] = 0;
     for (long a = (long)t0 * K + lane; a < (long)t * K; a += 32) {   // at most 7 K' entries
         const int x = topk_idx[a];
 #pragma unroll
@@ -325,10 +330,9 @@ __global__ void __launch_bounds__(256) gather_place_kernel(
         const int c = __reduce_add_sync(0xffffffffu, cnt[k]);
         rows[k] = -1;
         if (k < K) {
-            if (j[k] >= 0 && j[k] < N) {
-                const long r = (long)offsets[j[k]] + tile_base[(size_t)j[k] * n_tiles + tile] +
-                               hist[j[k]] + c;
-                if (r >= 0 && r < TK) rows[k] = (int)r;
+            if (seg0[k] >= 0) {
+                const long r = seg0[k] + hist[j[k]] + c;
+                if (r < TK) rows[k] = (int)r;
                 else bad = true;
             } else {
                 bad = true;
@@ -337,16 +341,8 @@ __global__ void __launch_bounds__(256) gather_place_kernel(
     }
     if (bad && lane == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
     write_places<KB>(m, t, rows, lane, perm_token, perm_slot);
-#pragma unroll
-    for (int i = 0; i < kHead; ++i) {
-        const int v = lane + 32 * i;
-        if (v < vec_per_row) {
-#pragma unroll
-            for (int k = 0; k < KB; ++k)
-                if (k < K && rows[k] >= 0) x_perm[(size_t)rows[k] * vec_per_row + v] = head[i];
-        }
-    }
-    for (int v = lane + 32 * kHead; v < vec_per_row; v += 32) {
+    const int vec_per_row = m.d * m.elem() / 16;
+    for (int v = lane; v < vec_per_row; v += 32) {
         const uint4 x = u[(size_t)t * vec_per_row + v];
 #pragma unroll
         for (int k = 0; k < KB; ++k)
