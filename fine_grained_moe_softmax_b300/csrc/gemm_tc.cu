@@ -275,6 +275,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const int total = prefix[gt.n_groups];
+    const int s_tiles = prefix[1];   // the shared group's tiles come first in tile order
+    const int s_start = shared_start(total, s_tiles, n_units, args.k_blocks_s > args.k_blocks_r);
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer ----
@@ -284,7 +286,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             long issued = 0;
             bool ok = true;
             for (int t = unit; t < total && ok; t += n_units) {
-                const TileInfo ti = decode_tile<TM>(t, prefix, rows_s, row0_s, gt);
+                const TileInfo ti =
+                    decode_tile<TM>(tile_at(t, s_tiles, s_start), prefix, rows_s, row0_s, gt);
                 const bool sh = ti.group == 0;
                 const CUtensorMap* am = sh ? &args.a_s : &args.a_r;
                 const CUtensorMap* bm = sh ? &args.b_s : &args.b_r;
@@ -354,7 +357,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true, any = false;
             for (int t = unit; t < total && ok; t += n_units) {
-                const TileInfo ti = decode_tile<TM>(t, prefix, rows_s, row0_s, gt);
+                const TileInfo ti =
+                    decode_tile<TM>(tile_at(t, s_tiles, s_start), prefix, rows_s, row0_s, gt);
                 const int kb_n = ti.group == 0 ? args.k_blocks_s : args.k_blocks_r;
                 if (!wait_phase<PAIR>(ptx::smem_addr(&tempty[acc]), acc_phase ^ 1, abort_flag,
                                       args.status))
@@ -418,7 +422,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = unit; t < total; t += n_units) {
-            const TileInfo ti = decode_tile<TM>(t, prefix, rows_s, row0_s, gt);
+            const TileInfo ti =
+                decode_tile<TM>(tile_at(t, s_tiles, s_start), prefix, rows_s, row0_s, gt);
             const bool sh = ti.group == 0;
             const int wrow0 = ti.m_blk * TM + row_off + quarter * 32;   // the warp's first row
             const int r = wrow0 + lane;                                  // row inside the group

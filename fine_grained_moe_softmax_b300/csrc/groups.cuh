@@ -73,6 +73,23 @@ __device__ __forceinline__ void build_tile_prefix(int* prefix, int* rows_s, int*
     __syncthreads();
 }
 
+// Tile t of a persistent launch runs on unit t mod U (U = units of the grid), so with R = total
+// mod U > 0 the units below R get one tile more. When the shared group's S tiles are longer than
+// the routed ones (a longer K loop: the down GEMM, whose shared group is K_s experts deep) and few
+// (S <= U - R and S <= total - R, as in a decode-sized batch), they are moved to positions
+// R .. R+S-1, onto units with one tile less; the routed tiles keep their order around them.
+// shared_start() gives R (0: positions are tile indices), tile_at() the tile of position p.
+__device__ __forceinline__ int shared_start(int total, int s_tiles, int units, bool shared_longer) {
+    if (!shared_longer || s_tiles <= 0 || units <= 0) return 0;
+    const int rem = total % units;   // positions 0 .. R-1 need R routed tiles
+    return (rem > 0 && rem + s_tiles <= units && rem + s_tiles <= total) ? rem : 0;
+}
+__device__ __forceinline__ int tile_at(int p, int s_tiles, int start) {
+    if (start == 0) return p;
+    if (p < start) return s_tiles + p;
+    return p < start + s_tiles ? p - start : p;
+}
+
 template <int BM>
 __device__ __forceinline__ TileInfo decode_tile(int t, const int* prefix, const int* rows_s,
                                                 const int* row0_s, const GroupTiles& gt) {
