@@ -217,12 +217,13 @@ __global__ void gather_cta_kernel(Dims m, const uint4* __restrict__ u,
     }
 }
 
-// The rows of token t's assignments, by one warp, for the layer call's gather (which so takes over
-// the work of perm_scatter_kernel, off the path that the shared experts' GEMM waits for). With
-// b = t / 128, the row of (t, k) is offsets[j] + tile_base[j][b] + the number of assignments of
-// the tile's earlier tokens to j = topk_idx[t][k]: a token chooses an expert at most once and
-// assignments are ordered token-major, so these are the rows of perm_scatter_kernel's counting
-// sort, bit for bit. rows[k] = -1 (and `bad`) for an expert id or a row out of range.
+// The rows of token t's assignments, computed by one warp. The layer call's gather places the
+// assignments itself, which takes perm_scatter_kernel's work off the path that the shared
+// experts' GEMM waits for. With b = t / 128, the row of (t, k) is offsets[j] + tile_base[j][b] +
+// the number of assignments of the tile's earlier tokens to j = topk_idx[t][k]: a token chooses
+// an expert at most once and assignments are ordered token-major, so these are the rows of
+// perm_scatter_kernel's counting sort, bit for bit. rows[k] = -1 (and `bad`) for an expert id or
+// a row out of range.
 template <int KB>
 __device__ __forceinline__ void place_token(const Dims& m, int t, const int* __restrict__ topk_idx,
                                             const int* __restrict__ offsets,
