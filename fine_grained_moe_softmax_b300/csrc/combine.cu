@@ -59,8 +59,6 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims m, const E* __restric
                                                       E* __restrict__ h, int* status,
                                                       long row_limit) {
     constexpr int VN = Vec<E>::n;
-    pdl_wait();
-    pdl_trigger();
     const int t = blockIdx.x;
     const long TK = row_limit;   // rows of y_r
     int rows[KMAX];
@@ -83,10 +81,18 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims m, const E* __restric
             }
         }
     }
+    // the routing tables (written at least three launches earlier: the predecessor that this
+    // kernel may overlap, the down GEMM, waited for them before it let this kernel start) and u
+    // are read before the wait for that predecessor's outputs, y_r and y_s
+    const int c0 = threadIdx.x * VN;
+    uint4 raw_u0 = make_uint4(0u, 0u, 0u, 0u);
+    if (c0 < m.d) raw_u0 = *reinterpret_cast<const uint4*>(u + (size_t)t * m.d + c0);
+    pdl_wait();
+    pdl_trigger();
     if (bad && threadIdx.x == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
     const bool shared = m.shared_active();
-    for (int c = threadIdx.x * VN; c < m.d; c += blockDim.x * VN) {
-        uint4 raw_u = *reinterpret_cast<const uint4*>(u + (size_t)t * m.d + c);
+    for (int c = c0; c < m.d; c += blockDim.x * VN) {
+        uint4 raw_u = c == c0 ? raw_u0 : *reinterpret_cast<const uint4*>(u + (size_t)t * m.d + c);
         uint4 raw_s = shared ? *reinterpret_cast<const uint4*>(y_s + (size_t)t * m.d + c) : raw_u;
         uint4 raw_r[KMAX];
 #pragma unroll

@@ -194,10 +194,14 @@ __global__ void gather_kernel(Dims m, const uint4* __restrict__ u, const int* __
 __global__ void gather_cta_kernel(Dims m, const uint4* __restrict__ u,
                                   const int* __restrict__ perm_slot, uint4* __restrict__ x_perm,
                                   int* status, long TK) {
-    pdl_wait();
-    pdl_trigger();
     const int t = blockIdx.x;
     const int vec_per_row = m.d * m.elem() / 16;
+    // u (an input of the call, complete before its first launch) is read before the wait for
+    // the predecessor's outputs, perm_slot
+    uint4 x0 = make_uint4(0u, 0u, 0u, 0u);
+    if ((int)threadIdx.x < vec_per_row) x0 = u[(size_t)t * vec_per_row + threadIdx.x];
+    pdl_wait();
+    pdl_trigger();
     int rows[kMaxTopK];
     bool bad = false;
 #pragma unroll
@@ -210,7 +214,7 @@ __global__ void gather_cta_kernel(Dims m, const uint4* __restrict__ u,
     }
     if (bad && threadIdx.x == 0) set_status(status, MOE_ERR_CORRUPT_INPUT);
     for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
-        const uint4 x = u[(size_t)t * vec_per_row + v];
+        const uint4 x = v == (int)threadIdx.x ? x0 : u[(size_t)t * vec_per_row + v];
 #pragma unroll
         for (int k = 0; k < kMaxTopK; ++k)
             if (k < m.K && rows[k] >= 0) x_perm[(size_t)rows[k] * vec_per_row + v] = x;
