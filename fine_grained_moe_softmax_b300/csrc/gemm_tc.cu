@@ -128,6 +128,7 @@ struct TcArgs {
     __nv_bfloat16* pre_s;         // unit-major (see pre_unit)
     int pre_rows_r, pre_rows_s;   // rows of the two buffers
     int* status;
+    int preload;                  // see GroupedGemm::preload
 };
 
 // Output staging of the box-store epilogues: per epilogue warp two boxes of 32 rows x 32 bf16
@@ -263,10 +264,20 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             ptx::tmem_relinquish();
         }
     }
-    pdl_wait();
-    pdl_trigger();
+    // with preload, the tile tables are built before the wait for the preceding launch and the
+    // producer thread waits on its own, after it has issued the first tile's weight loads
+    const bool preload = !PAIR && args.preload != 0;
+    const bool producer = warp == 0 && lane == 0;
+    if (!preload) {
+        pdl_wait();
+        pdl_trigger();
+    }
     build_tile_prefix<TM>(prefix, rows_s, row0_s, args.offsets, gt, args.counts,
                           args.status);   // syncs
+    if (preload && !producer) {
+        pdl_wait();
+        pdl_trigger();
+    }
     ptx::tc_fence_before();
     if constexpr (PAIR)
         ptx::cluster_sync();   // both CTAs' barriers are initialised before either uses the other's
@@ -285,6 +296,27 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             uint32_t phase = 0;
             long issued = 0;
             bool ok = true;
+            int pre = 0;   // K blocks of the first tile whose weights were loaded before the wait
+            if (preload) {
+                if (unit < total) {
+                    const TileInfo ti = decode_tile<TM>(tile_at(unit, s_tiles, s_start), prefix,
+                                                        rows_s, row0_s, gt);
+                    const bool sh = ti.group == 0;
+                    const int kb_n = sh ? args.k_blocks_s : args.k_blocks_r;
+                    const int b_y = (sh ? 0 : (ti.group - 1) * args.b_rows_per_expert) +
+                                    ti.n_blk * BN;
+                    pre = kb_n < STAGES ? kb_n : STAGES;
+                    // a fresh ring: stage kb is free; its barrier expects the A box as well
+                    for (int kb = 0; kb < pre; ++kb) {
+                        const uint32_t fb = ptx::smem_addr(&full[kb]);
+                        ptx::mbar_arrive_expect_tx(fb, S::a_bytes + S::b_bytes);
+                        ptx::tma_load_2d(ptx::smem_addr(b_ring + kb * S::b_bytes),
+                                         sh ? &args.b_s : &args.b_r, kb * BK, b_y, fb);
+                    }
+                }
+                pdl_wait();
+                pdl_trigger();
+            }
             for (int t = unit; t < total && ok; t += n_units) {
                 const TileInfo ti =
                     decode_tile<TM>(tile_at(t, s_tiles, s_start), prefix, rows_s, row0_s, gt);
@@ -296,6 +328,16 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                 const int b_y = (sh ? 0 : (ti.group - 1) * args.b_rows_per_expert) + ti.n_blk * BN +
                                 (PAIR ? (int)crank * (BN / 2) : 0);
                 for (int kb = 0; kb < kb_n; ++kb) {
+                    if (t == unit && kb < pre) {   // the weights are in flight: the A box only
+                        ptx::tma_load_2d(ptx::smem_addr(a_ring + stage * S::a_bytes), am, kb * BK,
+                                         a_y, ptx::smem_addr(&full[stage]));
+                        ++issued;
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                        continue;
+                    }
                     if (!wait_phase<PAIR>(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag,
                                           args.status)) {
                         ok = false;
@@ -762,6 +804,7 @@ cudaError_t run_gemm(const GroupedGemm& g, int* status, cudaStream_t st) {
     a.pre_rows_r = g.pre_rows_r;
     a.pre_rows_s = g.pre_rows_s;
     a.status = status;
+    a.preload = g.preload;
     if (EPI != 2) {   // box-store maps of the outputs (the slot of an absent group copies the other)
         // EPI 1 writes one activation per gate/up column pair: half the GEMM's columns
         const int div = EPI == 1 ? 2 : 1, box_cols = EPI == 1 ? 16 : 32;
@@ -828,6 +871,11 @@ cudaError_t launch_expert_gemms(const Dims& m, const void* u, const void* x_perm
     gu.T_shared = m.T;
     gu.offsets = offsets;
     gu.max_routed_rows = (long)TK;
+    // the offsets come from the router or the finalize kernel, ahead of the gather (or from the
+    // caller), so both GEMMs may load their first weights while the preceding launch finishes.
+    // Done for decode-sized batches, whose GEMMs stream weights and follow short launches (at
+    // larger T no gain was measured)
+    gu.preload = m.T <= 64 ? 1 : 0;
     gu.a_r = x_perm;
     gu.a_s = u;
     gu.b_r = pk + P.gu_r * 2;

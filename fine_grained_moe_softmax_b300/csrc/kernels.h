@@ -125,6 +125,10 @@ struct GroupedGemm {
     const int* offsets;
     const int* counts;
     long max_routed_rows;
+    // offsets / counts come from a launch at least two before this one, or from before the
+    // call: the producer may then read them, and load the first tile's weights, before it waits
+    // for the preceding launch (single-CTA tiles only)
+    int preload = 0;
 };
 cudaError_t run_grouped_gemm(const GroupedGemm& g, int epilogue, int* status, cudaStream_t st);
 
