@@ -320,15 +320,16 @@ __device__ __noinline__ void route_tile(const RouterParams& a, uint32_t tmem, ui
                     }
             }
         }
+        // bias_s holds zeros past N', so the padding columns keep their (unused) raw values
 #pragma unroll
-        for (int i = 0; i < 8; ++i) zc[(c + i) * RBM + row] = __uint_as_float(v[i]);
-        const int c_end = min(c + 8, N);
-#pragma unroll 1
-        for (int j = c; j < c_end; ++j) {
-            const float z = zc[j * RBM + row] + bias_s[j];
+        for (int i = 0; i < 8; ++i) {
+            const int j = c + i;
+            const float z = __uint_as_float(v[i]) + bias_s[j];
             zc[j * RBM + row] = z;
-            mloc = fmaxf(mloc, z);
-            top.push(z, j);
+            if (j < N) {
+                mloc = fmaxf(mloc, z);
+                top.push(z, j);
+            }
         }
     }
     red_max[h * RBM + row] = mloc;
