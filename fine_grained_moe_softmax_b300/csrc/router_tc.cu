@@ -9,10 +9,11 @@
 // the centroids stream through a TMA ring into tcgen05.mma (M = 128, N = N' rounded up to 32),
 // accumulating fp32 logits in TMEM. A ring stage holds up to four 64-deep K chunks, and each
 // operand of a stage is one 3D tensor copy (a copy costs about the same whatever its size, so
-// fewer, larger copies move more bytes per cycle). When there are few tiles (decode-sized batches), a cluster of
-// C CTAs shares a tile, each over 1/C of d; the other CTAs leave their partial logits in their
-// shared memory and the first adds them to its own, in rank order, through distributed shared
-// memory, so the sum does not depend on timing.
+// fewer, larger copies move more bytes per cycle). When there are few tiles (decode-sized
+// batches), a cluster of C CTAs shares a tile, each over 1/C of d; the other CTAs leave their
+// partial logits in their shared memory and the first adds them to its own, in rank order,
+// through distributed shared memory, so the sum does not depend on timing. The other CTAs exit
+// once the first CTA's threads have read them (a split cluster barrier).
 //
 // Sixteen epilogue warps route the tile: four per TMEM lane quarter (warp w reads lanes
 // 32*(w%4) .. +31), each over a quarter of the expert columns. A thread owns one token of one
@@ -22,7 +23,9 @@
 // (added in slice order) the denominator, and a shuffle transpose the tile's per-expert sums of
 // affinities in a fixed order. The four slice lists of a token are merged by four lanes, one list
 // each, in K' rounds of a 4-way maximum whose ties go to the lower slice (the lower indices);
-// those lanes then write the token's experts and gates and count the tile's histogram.
+// those lanes then write the token's experts and gates and count the tile's histogram. The
+// epilogue runs once per launch and its instructions are fetched cold, so it is one non-inlined
+// function with rolled loops; warps whose 32 tokens are all past the batch skip its phases.
 #include <math.h>
 
 #include "common.cuh"
