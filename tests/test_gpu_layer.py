@@ -104,6 +104,8 @@ def _custom(**kw):
     dict(d=128, inter=320, T=200),                  # 160-column gate/up tiles
     dict(d=256, inter=128, T=40),                   # <= 64 tokens: 64-row A tiles, 5 stages
     dict(n_routed=256, top_k=8, n_groups=8, T=300), # widest router
+    # the placing gather in its one-CTA-per-token form (129 .. 296 tokens), 5 <= K' <= 8
+    dict(n_routed=64, top_k=6, n_groups=8, d=512, inter=64, T=250),
     # router column slices with ragged ends (n_pad 224, 128, 64 over 200, 100, 40 experts), stages
     # of 2, 3 and 4 K chunks with a shorter last stage, one-tile and cluster-split tiles
     dict(n_routed=200, top_k=8, n_groups=8, d=640, T=300),
