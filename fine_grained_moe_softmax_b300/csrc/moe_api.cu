@@ -368,7 +368,7 @@ int moe_layer_forward(const moe_config* cfg, const void* u, const void* centroid
     }
     mk.mark(2);
     // With shared experts, the shared group's gate/up GEMM needs only u. The permuted token rows
-    // are then placed and gathered on a side stream while it runs (the gather needs no shared
+    // are then placed and gathered on a side stream while it runs (the gather needs 1 KB of shared
     // memory, so its CTAs fit beside the GEMM's, and the GEMM leaves most of the memory bandwidth
     // idle); the routed groups' gate/up follows once they are ready. The gather stage of the
     // profile is then timed on the side stream and the gate/up stage is the rest of the gate/up
