@@ -587,6 +587,19 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
     }
     pdl_wait();
     pdl_trigger();
+    // the producer thread initialised the barriers itself: it issues the ring's first stages
+    // before the block-wide sync, so that these loads overlap the TMEM allocation and the rest of
+    // the set-up (the ring is fresh, every stage is free)
+    int pre_loads = 0;
+    if (warp == 0 && lane == 0) {
+        for (int kb = kb_begin; kb < kb_end && pre_loads < stages; kb += kc, ++pre_loads) {
+            const uint32_t fb = ptx::smem_addr(&full[pre_loads]);
+            uint8_t* st = base + pre_loads * stage_bytes;
+            ptx::mbar_arrive_expect_tx(fb, stage_bytes);
+            ptx::tma_load_3d(ptx::smem_addr(st), &a.a, 0, tile * RBM, kb, fb);
+            ptx::tma_load_3d(ptx::smem_addr(st + kc * RBM * RBK * 2), &a.b, 0, 0, kb, fb);
+        }
+    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -595,11 +608,11 @@ __global__ void __launch_bounds__(router_threads(BWD), 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer ----
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int issued = 0;
+            int stage = pre_loads % stages;
+            uint32_t phase = pre_loads == stages ? 1u : 0u;
+            int issued = pre_loads;
             bool ok = true;
-            for (int kb = kb_begin; kb < kb_end; kb += kc) {
+            for (int kb = kb_begin + pre_loads * kc; kb < kb_end; kb += kc) {
                 if (!wait_phase(ptx::smem_addr(&empty[stage]), phase ^ 1, abort_flag, status)) {
                     ok = false;
                     break;
